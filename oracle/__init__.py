@@ -1,0 +1,10 @@
+"""CPU fp64 oracle for exact attention (test infrastructure only).
+
+Imported by the tests, the smoke check and the bench's CPU-baseline leg; the
+product path never imports it.
+"""
+from .attention import (BLOCK, backward, forward, head_backward, head_backward_jacobian,
+                        head_forward, head_probs, loss, to_f64, visible)
+
+__all__ = ["BLOCK", "backward", "forward", "head_backward", "head_backward_jacobian",
+           "head_forward", "head_probs", "loss", "to_f64", "visible"]
