@@ -1,0 +1,160 @@
+"""ctypes binding of libfa.so: argument marshalling only.
+
+Every step of the attention computation runs in the CUDA kernels behind the
+C-ABI (include/fa.h). This module turns torch tensors into device pointers
+and streams, allocates outputs with torch, and raises on a non-zero status.
+There is no CPU path: a missing library or a non-CUDA tensor is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+_lib = None
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOUT = range(5)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_fwd_kpad": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P]),
+    "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P,
+                    ctypes.c_size_t, _P]),
+    "fa_blocksparse_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P]),
+    "fa_device_status": (_I, []),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_selftest_wait_timeout": (_I, [ctypes.c_longlong, _P]),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "exact_io_aware_11_gb300.build.build() (needs nvcc)")
+        handle = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def _stream_ptr(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _check_qkv(*ts):
+    for t in ts:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("exact attention runs on CUDA tensors only")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("expected contiguous bf16 tensors of shape [B, H, N, d]")
+        if t.shape != ts[0].shape:
+            raise ValueError("q, k, v (and o, dout) must have the same shape")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _raise(rc: int, where: str):
+    if rc != FA_OK:
+        raise FaError(rc, where)
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, kv_len=None,
+            out=None, lse=None, stream=None):
+    """O, LSE = exact attention forward (fa_fwd / fa_fwd_kpad)."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if kv_len is not None and (kv_len.dtype != torch.int32 or not kv_len.is_cuda):
+        raise ValueError("kv_len must be a CUDA int32 tensor of shape [B]")
+    rc = lib().fa_fwd_kpad(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                           B, H, N, d, int(bool(causal)), scale, _ptr(kv_len), _stream_ptr(stream))
+    _raise(rc, "fa_fwd_kpad")
+    return o, l
+
+
+def blocksparse_forward(q, k, v, block_mask, scale: float | None = None, block_size: int = 128,
+                        out=None, lse=None, stream=None):
+    """O, LSE = block-sparse exact attention forward (fa_blocksparse_fwd)."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if block_mask.dtype != torch.uint8 or not block_mask.is_cuda or not block_mask.is_contiguous():
+        raise ValueError("block_mask must be a contiguous CUDA uint8 tensor [nb, nb]")
+    nb = (N + block_size - 1) // block_size
+    if tuple(block_mask.shape) != (nb, nb):
+        raise ValueError(f"block_mask must have shape ({nb}, {nb})")
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = lib().fa_blocksparse_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  l.data_ptr(), B, H, N, d, scale, block_mask.data_ptr(),
+                                  int(block_size), _stream_ptr(stream))
+    _raise(rc, "fa_blocksparse_fwd")
+    return o, l
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+             kv_len=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of L = sum(dout * O) (fa_bwd). `workspace` is an optional
+    uint8 CUDA tensor of at least bwd_workspace_bytes(...) bytes."""
+    _check_qkv(q, k, v, o, dout)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if kv_len is not None and (kv_len.dtype != torch.int32 or not kv_len.is_cuda):
+        raise ValueError("kv_len must be a CUDA int32 tensor of shape [B]")
+    rc = lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                      lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                      int(bool(causal)), scale, _ptr(kv_len), ws.data_ptr(), ws.numel(),
+                      _stream_ptr(stream))
+    _raise(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def device_status() -> int:
+    """Read-and-clear the device-side status word (call after a synchronize)."""
+    return int(lib().fa_device_status())
+
+
+def selftest_wait_timeout(limit_cycles: int, stream=None) -> int:
+    return int(lib().fa_selftest_wait_timeout(int(limit_cycles), _stream_ptr(stream)))

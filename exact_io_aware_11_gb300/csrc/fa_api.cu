@@ -1,0 +1,281 @@
+// C-ABI of libfa.so (declared in include/fa.h): argument validation, TMA
+// descriptor encoding, workspace carving and dispatch to the kernels on the
+// caller's stream. Holds no state beyond one device-side status word per
+// device and a cached driver entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Per-device: address of the status word and whether the device is sm_103.
+struct DeviceInfo {
+  int* status = nullptr;
+  int supported = -1;  // -1 unknown
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mu;
+
+int current_device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_devices_mu);
+  DeviceInfo& info = g_devices[dev];
+  if (info.supported < 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    info.supported = (major == 10 && minor == 3) ? 1 : 0;
+  }
+  if (!info.supported) return FA_ERR_UNSUPPORTED;
+  if (info.status == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FA_ERR_CUDA;
+    info.status = static_cast<int*>(p);
+  }
+  *out = info;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// [B*H, N, d] bf16 as a 3-D tensor map; box = 64 columns (128 bytes) x 128 rows
+// x 1 head, 128-byte swizzle, zero fill outside the tensor (ragged N).
+bool encode_bhnd(CUtensorMap* map, const void* base, int B, int H, int N, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(B) * static_cast<cuuint64_t>(H)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlock), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int check_common(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 65535LL * 65535LL) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t tensor_bytes(int B, int H, int N, int d, size_t elem) {
+  return static_cast<size_t>(B) * H * N * d * elem;
+}
+
+int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, int causal, float scale, const int32_t* kv_len,
+               const uint8_t* block_mask, cudaStream_t stream) {
+  int st = check_common(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  const size_t tb = tensor_bytes(B, H, N, d, 2), lb = tensor_bytes(B, H, N, 1, 4);
+  const void* ins[3] = {q, k, v};
+  for (const void* in : ins)
+    if (overlaps(o, tb, in, tb) || overlaps(lse, lb, in, tb)) return FA_ERR_INVALID_ARG;
+  if (overlaps(o, tb, lse, lb)) return FA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  st = current_device_info(&dev);
+  if (st != FA_OK) return st;
+  FwdLaunch a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bhnd(&a.tm_q, q, B, H, N, d) || !encode_bhnd(&a.tm_k, k, B, H, N, d) ||
+      !encode_bhnd(&a.tm_v, v, B, H, N, d))
+    return FA_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.kv_len = kv_len;
+  a.block_mask = block_mask;
+  a.status = dev.status;
+  a.wait_limit = kWaitLimitCycles;
+  return launch_fwd(a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
+  BwdWorkspace w{};
+  const size_t npad = static_cast<size_t>((N + kBlock - 1) / kBlock) * kBlock;
+  const size_t rows = static_cast<size_t>(B) * H * npad;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  w.dq_off = 0;
+  w.lse2_off = up(rows * d * 4);
+  w.delta_off = w.lse2_off + up(rows * 4);
+  w.total = w.delta_off + up(rows * 4);
+  return w;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, int causal, float scale, struct CUstream_st* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, N, d, causal, scale, nullptr, nullptr, stream);
+}
+
+int fa_fwd_kpad(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, int d, int causal, float scale, const int32_t* kv_len,
+                struct CUstream_st* stream) {
+  return fwd_common(q, k, v, o, lse, B, H, N, d, causal, scale, kv_len, nullptr, stream);
+}
+
+int fa_blocksparse_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, float scale, const uint8_t* block_mask, int block_size,
+                       struct CUstream_st* stream) {
+  if (block_mask == nullptr) return FA_ERR_INVALID_ARG;
+  if (block_size != kBlock) return FA_ERR_UNSUPPORTED;
+  return fwd_common(q, k, v, o, lse, B, H, N, d, 0, scale, nullptr, block_mask, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  return bwd_workspace_layout(B, H, N, d).total;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+           float scale, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+           struct CUstream_st* stream) {
+  int st = check_common(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+  for (const void* p : all)
+    if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  const BwdWorkspace ws = bwd_workspace_layout(B, H, N, d);
+  if (workspace_bytes < ws.total) return FA_ERR_INVALID_ARG;
+  const size_t tb = tensor_bytes(B, H, N, d, 2), lb = tensor_bytes(B, H, N, 1, 4);
+  const void* ins[] = {q, k, v, o, dout};
+  void* outs[] = {dq, dk, dv};
+  for (void* out : outs) {
+    for (const void* in : ins)
+      if (overlaps(out, tb, in, tb)) return FA_ERR_INVALID_ARG;
+    if (overlaps(out, tb, lse, lb) || overlaps(out, tb, workspace, ws.total))
+      return FA_ERR_INVALID_ARG;
+  }
+  if (overlaps(dq, tb, dk, tb) || overlaps(dq, tb, dv, tb) || overlaps(dk, tb, dv, tb))
+    return FA_ERR_INVALID_ARG;
+  for (const void* in : ins)
+    if (overlaps(workspace, ws.total, in, tb)) return FA_ERR_INVALID_ARG;
+  if (overlaps(workspace, ws.total, lse, lb)) return FA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  st = current_device_info(&dev);
+  if (st != FA_OK) return st;
+  BwdLaunch a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bhnd(&a.tm_q, q, B, H, N, d) || !encode_bhnd(&a.tm_k, k, B, H, N, d) ||
+      !encode_bhnd(&a.tm_v, v, B, H, N, d) || !encode_bhnd(&a.tm_do, dout, B, H, N, d))
+    return FA_ERR_CUDA;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.kv_len = kv_len;
+  a.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
+  a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
+  a.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
+  a.status = dev.status;
+  a.wait_limit = kWaitLimitCycles;
+  return launch_bwd(a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_device_status(void) {
+  DeviceInfo dev;
+  const int st = current_device_info(&dev);
+  if (st != FA_OK) return st == FA_ERR_UNSUPPORTED ? FA_ERR_UNSUPPORTED : FA_ERR_CUDA;
+  int value = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&value, g_status_word, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  return value;
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    default: return "FA_UNKNOWN_STATUS";
+  }
+}
+
+int fa_selftest_wait_timeout(long long limit_cycles, struct CUstream_st* stream) {
+  if (limit_cycles < 1) return FA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  const int st = current_device_info(&dev);
+  if (st != FA_OK) return st;
+  return launch_wait_selftest(dev.status, limit_cycles, stream) == cudaSuccess ? FA_OK
+                                                                               : FA_ERR_CUDA;
+}
+
+}  // extern "C"

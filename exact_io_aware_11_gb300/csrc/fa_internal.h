@@ -1,0 +1,60 @@
+// Host-side launch descriptions shared by the C-ABI layer and the kernels'
+// translation units. Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+// Budget of one bounded device wait, in SM clock cycles (about a second).
+constexpr long long kWaitLimitCycles = 2000000000LL;
+
+// Rows of one Q tile and one K/V tile (the 128 x 128 block of the method).
+constexpr int kBlock = 128;
+
+struct FwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H, N, d], box 64 x 128 x 1, 128B swizzle
+  void* o;
+  float* lse;
+  int B, H, N, d;
+  int causal;
+  float scale;
+  const int32_t* kv_len;      // device [B] or nullptr
+  const uint8_t* block_mask;  // device [nb, nb] or nullptr
+  int* status;
+  long long wait_limit;
+};
+
+struct BwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as above
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, H, N, d;
+  int causal;
+  float scale;
+  const int32_t* kv_len;
+  float* dq_acc;   // workspace: fp32 [B*H, Npad, d]
+  float* lse2;     // workspace: fp32 [B*H, Npad]  (LSE * log2 e; +inf on padding rows)
+  float* delta;    // workspace: fp32 [B*H, Npad]  (rowsum(dO * O); 0 on padding rows)
+  int* status;
+  long long wait_limit;
+};
+
+// Workspace carving shared by fa_bwd_workspace_bytes and fa_bwd.
+struct BwdWorkspace {
+  size_t dq_off, lse2_off, delta_off, total;
+};
+BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d);
+
+cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_wait_selftest(int* status, long long limit_cycles, cudaStream_t stream);
+
+}  // namespace fa

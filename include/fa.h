@@ -1,0 +1,126 @@
+/*
+ * fa.h -- C-ABI of libfa.so: exact scaled-dot-product attention on one
+ * GB300 (sm_103a), forward, backward and block-sparse forward.
+ *
+ * What is computed (per batch b and head h; Q, K, V, dO in R^{N x d}):
+ *   S = scale * Q K^T + M,  P = softmax(S) row-wise,  O = P V,
+ *   LSE_i = ln sum_j exp(S_ij)  (natural log, scale included).
+ * This is standard attention as stated in the condensed FlashAttention paper
+ * (sample_paper.md, section 2 "Background"; shapes "Q: N x d, K^T: d x N,
+ * QK^T: N x N, sm(QK^T)V: N x d" in the aggregator page's figure captions).
+ * The kernels tile Q, K, V through on-chip memory and rescale the softmax
+ * incrementally, so S and P never reach HBM (sample_paper.md section 3,
+ * "Tiling" and "Softmax rescaling / recomputation"; Figure 1 of the Medium
+ * article "No More Quadratic Complexity for Transformers"). The result is
+ * exact up to floating-point rounding.
+ *
+ * Conventions common to every entry point
+ *   - Tensors are DEVICE pointers, row-major [B, H, N, d] with d fastest and
+ *     no padding between rows or heads. q, k, v, o, dout, dq, dk, dv are bf16
+ *     (passed as void*); lse is fp32 [B, H, N].
+ *   - Base addresses must be 16-byte aligned. d must be 64 or 128. Any N >= 1.
+ *   - The mask M_ij is 0 or -inf: causal keeps j <= i; kv_len (optional) keeps
+ *     j < kv_len[b] for every query row of batch b; a block mask keeps whole
+ *     128 x 128 blocks. A query row that sees no key gets O = 0 and
+ *     LSE = -inf (and zero gradients).
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Outputs are valid once the stream is synchronised. Inputs are only read.
+ *   - Ownership: the caller owns every buffer. The library never allocates or
+ *     frees device memory; the backward pass takes a caller-provided
+ *     workspace whose size is linear in N (fa_bwd_workspace_bytes).
+ *   - Errors: arguments are validated before anything is launched and
+ *     nothing is written on error. FA_ERR_INVALID_ARG: a NULL pointer, B, H
+ *     or N < 1, non-finite scale, a misaligned base address, an output that
+ *     overlaps an input, or a workspace that is too small. FA_ERR_UNSUPPORTED:
+ *     d not in {64, 128}, block_size != 128, or a device that is not sm_103.
+ *     FA_ERR_CUDA: a CUDA call or launch failed. FA_ERR_DEVICE_TIMEOUT is
+ *     reported by fa_device_status() when a bounded device-side wait expired.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_CUDA = 3,
+  FA_ERR_DEVICE_TIMEOUT = 4
+} fa_status;
+
+struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
+
+/* Forward pass: O = softmax(scale * Q K^T [+ causal mask]) V and the per-row
+ * logsumexp LSE that the backward pass recomputes P from (sample_paper.md
+ * section 3: tiling, online softmax rescaling, "stored statistics").
+ *   q, k, v : bf16 [B,H,N,d] inputs;  o : bf16 [B,H,N,d] output;
+ *   lse     : fp32 [B,H,N] output;    causal : 0 or 1;  scale : finite. */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, int causal, float scale, struct CUstream_st* stream);
+
+/* Forward pass with key padding: as fa_fwd, and keys j >= kv_len[b] are
+ * masked for every query row of batch b. kv_len is a DEVICE int32 [B]
+ * (values are clamped to [0, N] on the device) or NULL for no padding. */
+int fa_fwd_kpad(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, int d, int causal, float scale, const int32_t* kv_len,
+                struct CUstream_st* stream);
+
+/* Bytes of workspace fa_bwd needs: an fp32 dQ accumulator plus two fp32
+ * per-row vectors (log2-scaled LSE and D = rowsum(dO * O)), each padded to a
+ * multiple of 128 rows per head. Linear in N (sample_paper.md section 4:
+ * memory linear in sequence length). Returns 0 for invalid sizes. */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/* Backward pass: gradients of L = sum(dO * O) with respect to Q, K, V. P is
+ * recomputed on chip from Q, K and the forward's LSE instead of being read
+ * from HBM (sample_paper.md section 3, "in the backward pass, the attention
+ * matrix is recomputed on-chip from stored statistics").
+ *   q, k, v, o, dout : bf16 [B,H,N,d] (o and lse from fa_fwd / fa_fwd_kpad
+ *                      with the same causal, scale and kv_len);
+ *   lse              : fp32 [B,H,N];
+ *   dq, dk, dv       : bf16 [B,H,N,d] outputs;
+ *   kv_len           : DEVICE int32 [B] or NULL (as in fa_fwd_kpad);
+ *   workspace        : DEVICE scratch of at least fa_bwd_workspace_bytes,
+ *                      16-byte aligned; its contents on entry are ignored. */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+           float scale, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
+           struct CUstream_st* stream);
+
+/* Block-sparse forward: fa_fwd (non-causal) where query block r attends only
+ * to key blocks c with block_mask[r * nb + c] != 0, nb = ceil(N / 128); the
+ * masked blocks are -inf and are skipped entirely, so IO and work fall in
+ * proportion to the sparsity (FlashAttention abstract, "block-sparse
+ * attention"; aggregator page, "IO complexity smaller ... proportional to the
+ * sparsity"). block_mask is a DEVICE uint8 [nb, nb] shared by all (b, h);
+ * block_size must be 128. */
+int fa_blocksparse_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int N, int d, float scale, const uint8_t* block_mask, int block_size,
+                       struct CUstream_st* stream);
+
+/* Device-side status of the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT
+ * if a bounded wait inside a kernel gave up since the last call. Reading
+ * clears it. Call only after synchronising the streams that ran the
+ * kernels. Returns FA_ERR_CUDA if the status word cannot be read. */
+int fa_device_status(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* fa_status_string(int status);
+
+/* Self-test of the device watchdog: launches one CTA that waits on an
+ * mbarrier nothing ever arrives on, with a budget of `limit_cycles` SM
+ * cycles. The wait gives up, the kernel records FA_ERR_DEVICE_TIMEOUT and
+ * returns; fa_device_status() then reports it. Nothing traps or hangs. */
+int fa_selftest_wait_timeout(long long limit_cycles, struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

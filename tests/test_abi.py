@@ -1,0 +1,153 @@
+"""Host-side checks of the C-ABI: the library builds and loads, exports every
+symbol include/fa.h declares, and rejects invalid arguments before touching
+the GPU. Fake pointers are used only in calls that must fail validation, so
+these tests are skipped where a GPU is present (the GPU tests cover the
+valid paths with real buffers)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from exact_io_aware_11_gb300 import build
+    build.build()
+    import exact_io_aware_11_gb300 as fa
+    return fa.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[a-z][\w\s\*]*?\b(fa_\w+)\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("fa_fwd", "fa_fwd_kpad", "fa_bwd", "fa_bwd_workspace_bytes", "fa_blocksparse_fwd",
+              "fa_device_status", "fa_status_string", "fa_selftest_wait_timeout"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    from exact_io_aware_11_gb300 import library_path
+    out = subprocess.run(["nm", "-D", "--defined-only", library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(fa_\w+)$", out, flags=re.M))
+    missing = [n for n in declared_symbols() if n not in exported]
+    assert not missing, missing
+    for n in declared_symbols():
+        assert hasattr(L, n)
+
+
+def test_status_strings(L):
+    import exact_io_aware_11_gb300 as fa
+    assert fa.status_string(0) == "FA_OK"
+    assert fa.status_string(4) == "FA_ERR_DEVICE_TIMEOUT"
+    assert fa.status_string(99) == "FA_UNKNOWN_STATUS"
+
+
+def test_workspace_bytes_is_linear_in_n(L):
+    import exact_io_aware_11_gb300 as fa
+    for d in (64, 128):
+        a = fa.bwd_workspace_bytes(2, 3, 1024, d)
+        b = fa.bwd_workspace_bytes(2, 3, 2048, d)
+        assert a == 2 * 3 * 1024 * (4 * d + 8)
+        assert b == 2 * a
+    # ragged N is padded to whole 128-row tiles
+    assert fa.bwd_workspace_bytes(1, 1, 130, 64) == fa.bwd_workspace_bytes(1, 1, 256, 64)
+    assert fa.bwd_workspace_bytes(1, 1, 0, 64) == 0
+    assert fa.bwd_workspace_bytes(1, 1, 128, 96) == 0
+
+
+needs_cpu = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="fake-pointer validation tests run on CPU-only hosts")
+
+A = 1 << 20          # fake, 16-byte aligned "device" addresses, never dereferenced
+SPAN = 1 << 28
+
+
+def ptrs(n):
+    return [A + i * SPAN for i in range(n)]
+
+
+@needs_cpu
+@pytest.mark.parametrize("case,expect", [
+    (dict(B=0), 1), (dict(H=0), 1), (dict(N=0), 1), (dict(d=96), 2), (dict(d=32), 2),
+    (dict(causal=2), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=-0.125), 1), (dict(scale=0.0), 1),
+    (dict(q=None), 1), (dict(o=None), 1), (dict(lse=None), 1), (dict(q=A + 8), 1),
+    (dict(o=A + 4 * SPAN + 2), 1),
+    (dict(o=A), 1),                         # output aliases q
+    (dict(lse=A + 3 * SPAN + 64), 1),        # lse overlaps o
+])
+def test_fwd_rejects_invalid(L, case, expect):
+    q, k, v, o, lse = ptrs(5)
+    args = dict(q=q, k=k, v=v, o=o, lse=lse, B=2, H=2, N=256, d=64, causal=0, scale=0.125)
+    args.update(case)
+    rc = L.fa_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["H"],
+                  args["N"], args["d"], args["causal"], args["scale"], None)
+    assert rc == expect
+
+
+@needs_cpu
+def test_kpad_rejects_misaligned_kv_len(L):
+    q, k, v, o, lse, kv = ptrs(6)
+    assert L.fa_fwd_kpad(q, k, v, o, lse, 1, 1, 128, 64, 0, 0.125, kv + 2, None) == 1
+
+
+@needs_cpu
+@pytest.mark.parametrize("case,expect", [
+    (dict(block_mask=None), 1), (dict(block_size=64), 2), (dict(d=80), 2), (dict(N=-1), 1),
+])
+def test_blocksparse_rejects_invalid(L, case, expect):
+    q, k, v, o, lse, m = ptrs(6)
+    args = dict(B=1, H=1, N=256, d=64, scale=0.125, block_mask=m, block_size=128)
+    args.update(case)
+    rc = L.fa_blocksparse_fwd(q, k, v, o, lse, args["B"], args["H"], args["N"], args["d"],
+                              args["scale"], args["block_mask"], args["block_size"], None)
+    assert rc == expect
+
+
+@needs_cpu
+@pytest.mark.parametrize("case,expect", [
+    (dict(ws_bytes=-1), 1),                  # one byte short
+    (dict(workspace=None), 1), (dict(dout=None), 1), (dict(dq=A), 1),   # dq aliases q
+    (dict(dk=A + 6 * SPAN), 1),              # dk aliases dq
+    (dict(workspace=A + 8 * SPAN + 8), 1),   # misaligned workspace
+    (dict(workspace=A + SPAN), 1),           # workspace overlaps k
+    (dict(d=256), 2), (dict(causal=-1), 1),
+])
+def test_bwd_rejects_invalid(L, case, expect):
+    q, k, v, o, do, lse, dq, dk, dv, ws = ptrs(10)
+    B, H, N, d = 2, 2, 256, case.get("d", 64)
+    need = L.fa_bwd_workspace_bytes(B, H, N, 64)
+    args = dict(q=q, k=k, v=v, o=o, dout=do, lse=lse, dq=dq, dk=dk, dv=dv, workspace=ws,
+                ws_bytes=0, causal=0)
+    args.update(case)
+    rc = L.fa_bwd(args["q"], args["k"], args["v"], args["o"], args["dout"], args["lse"],
+                  args["dq"], args["dk"], args["dv"], B, H, N, d, args["causal"], 0.125, None,
+                  args["workspace"], need + args["ws_bytes"], None)
+    assert rc == expect
+
+
+@needs_cpu
+def test_python_binding_refuses_cpu_tensors(L):
+    import exact_io_aware_11_gb300 as fa
+    x = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward(x, x, x)
+
+
+@needs_cpu
+def test_device_calls_fail_cleanly_without_gpu(L):
+    import exact_io_aware_11_gb300 as fa
+    # No device: status cannot be read, the self-test cannot launch.
+    assert fa.device_status() in (fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
+    assert L.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG

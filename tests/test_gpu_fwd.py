@@ -1,0 +1,116 @@
+"""Forward parity: CUDA path (through the C-ABI) vs the CPU fp64 oracle, on
+the same seeded bf16 inputs, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from _util import check_fwd, cuda, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def generic(B, H, N, d, causal=False, seed=0, kv=None):
+    w = W.Workload("generic", B, H, N, d, causal=causal, backward=False)
+    x = W.make_inputs(w, seed)
+    return w, x
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [128, 256, 384, 1000, 1])
+def test_fwd_small_sweep(fa, d, causal, N):
+    w, x = generic(2, 3, N, d, causal, seed=N + d)
+    o, lse = fa.forward(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, causal=causal)
+    check_fwd(o, lse, o_ref, l_ref, f"d={d} causal={causal} N={N}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_kv_len_edges(fa, d, causal):
+    N = 512
+    kv = torch.tensor([1, 127, 128, 129, 300, 512], dtype=torch.int32)
+    w, x = generic(len(kv), 2, N, d, causal, seed=7)
+    o, lse = fa.forward(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), causal=causal, scale=w.scale,
+                        kv_len=kv.cuda())
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, causal=causal, kv_len=kv.numpy())
+    check_fwd(o, lse, o_ref, l_ref, f"kv_len d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_fwd_tiny_workload(fa, seed):
+    w = W.WORKLOADS["tiny_fwd"]
+    x = W.make_inputs(w, seed)
+    o, lse = fa.forward(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, causal=w.causal)
+    check_fwd(o, lse, o_ref, l_ref, "tiny_fwd")
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "bert_large"])
+def test_fwd_full_size_short_sequences(fa, name):
+    w = W.WORKLOADS[name]
+    x = W.make_inputs(w, 0)
+    kv = cuda(x["kv_len"])
+    o, lse = fa.forward(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), causal=w.causal, scale=w.scale,
+                        kv_len=kv)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    kvn = None if x["kv_len"] is None else x["kv_len"].numpy()
+    o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, causal=w.causal, kv_len=kvn)
+    check_fwd(o, lse, o_ref, l_ref, name)
+
+
+def sample_rows(N, n=48, seed=0):
+    """Tile boundaries, first/last rows and a seeded random spread."""
+    g = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 1]
+    return np.unique(np.concatenate([fixed, g.integers(0, N, n)]))
+
+
+@pytest.mark.parametrize("N", [4096, 8192, 16384])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_full_size_long_context(fa, N, causal):
+    w = W.WORKLOADS[f"long_n{N}_{'causal' if causal else 'noncausal'}"]
+    x = W.make_inputs(w, 0)
+    o, lse = fa.forward(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    rows = sample_rows(N)
+    o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, causal=causal, rows=rows)
+    check_fwd(f64(o)[:, :, rows], f64(lse)[:, :, rows], o_ref, l_ref, w.name)
+
+
+def test_fwd_deterministic(fa):
+    w, x = generic(2, 4, 1024, 128, causal=True, seed=3)
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    o1, l1 = fa.forward(q, k, v, causal=True)
+    o2, l2 = fa.forward(q, k, v, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_fwd_kv_len_full_equals_dense(fa):
+    w, x = generic(2, 2, 384, 64, seed=4)
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    o1, l1 = fa.forward(q, k, v)
+    o2, l2 = fa.forward(q, k, v, kv_len=torch.full((2,), 384, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_fwd_rejects_misaligned_device_pointer(fa):
+    x = torch.zeros(1 * 1 * 128 * 64 + 1, dtype=torch.bfloat16, device="cuda")
+    good = x[:128 * 64]
+    bad = x[1:]
+    o = torch.empty(128 * 64, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(128, dtype=torch.float32, device="cuda")
+    rc = fa.lib().fa_fwd(bad.data_ptr(), good.data_ptr(), good.data_ptr(), o.data_ptr(),
+                         lse.data_ptr(), 1, 1, 128, 64, 0, 0.125, None)
+    assert rc == fa.FA_ERR_INVALID_ARG
