@@ -1,0 +1,445 @@
+"""Throughput of exact attention (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gpt2_small] [--no-sweep]
+
+One "step" is one pass of the hot path over one batch of the workload: the
+forward kernel, then the backward's preprocess, main and dQ-convert kernels.
+The headline workload is GPT-2-small-shaped causal attention (B=8, H=12,
+N=1024, d=64, bf16, seeded N(0,1) inputs). FLOPs per step follow the usual
+count: forward 4*B*H*N^2*d, backward 2.5x that, both halved for causal.
+
+Timing: inputs resident in HBM; W untimed warm-up steps; then K steps, each
+bracketed by CUDA events on the launching stream, with a 256 MiB buffer
+written between steps (outside the events) to flush the 126 MiB L2. Under
+torchrun every rank runs the same workload (independent (b, h) problems, no
+collective) and rank 0 prints the max-over-ranks time. The `e2e` leg repeats
+the step through the public API with pinned host buffers and the host<->
+device copies inside the timed region. `cpu_baseline` times the CPU fp64
+oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def flops(w: W.Workload, kv_len=None):
+    f = 4.0 * w.B * w.H * w.N * w.N * w.d
+    if w.causal:
+        f /= 2
+    return f, 2.5 * f
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- our arm
+class Step:
+    """Buffers and the staged calls of one fwd+bwd step on one workload."""
+
+    def __init__(self, fa, w: W.Workload, seed: int, dev):
+        self.fa, self.w = fa, w
+        x = W.make_inputs(w, seed)
+        self.host = x
+        self.q, self.k, self.v = (x[n].to(dev) for n in ("q", "k", "v"))
+        self.do = x["dout"].to(dev) if x["dout"] is not None else None
+        self.kv = x["kv_len"].to(dev) if x["kv_len"] is not None else None
+        self.mask = x["block_mask"].to(dev) if x["block_mask"] is not None else None
+        B, H, N, d = w.B, w.H, w.N, w.d
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.ws_bytes = fa.bwd_workspace_bytes(B, H, N, d)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.L = fa.lib()
+
+    def fwd(self, stream):
+        w, L = self.w, self.L
+        if self.mask is not None:
+            rc = L.fa_blocksparse_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                      self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
+                                      w.scale, self.mask.data_ptr(), 128, stream)
+        else:
+            rc = L.fa_fwd_kpad(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                               self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
+                               int(w.causal), w.scale,
+                               None if self.kv is None else self.kv.data_ptr(), stream)
+        assert rc == 0, rc
+
+    def bwd_stages(self, stream):
+        w, L = self.w, self.L
+        kv = None if self.kv is None else self.kv.data_ptr()
+        yield L.fa_bwd_preprocess(self.o.data_ptr(), self.do.data_ptr(), self.lse.data_ptr(),
+                                  w.B, w.H, w.N, w.d, self.ws.data_ptr(), self.ws_bytes, stream)
+        yield L.fa_bwd_main(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                            self.do.data_ptr(), self.dk.data_ptr(), self.dv.data_ptr(), w.B, w.H,
+                            w.N, w.d, int(w.causal), w.scale, kv, self.ws.data_ptr(),
+                            self.ws_bytes, stream)
+        yield L.fa_bwd_dq_convert(self.dq.data_ptr(), w.B, w.H, w.N, w.d, self.ws.data_ptr(),
+                                  self.ws_bytes, stream)
+
+
+KERNELS = ["fwd", "bwd_pre", "bwd_main", "dq_convert"]
+
+
+def time_steps(step: Step, steps: int, warmup: int, flush, backward=True):
+    """Returns per-kernel lists of milliseconds (K entries each)."""
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    n_ev = 5 if backward else 2
+    times = {k: [] for k in KERNELS[:n_ev - 1]}
+
+    def one(record):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] if record else None
+        if record:
+            evs[0].record(stream)
+        step.fwd(sp)
+        if record:
+            evs[1].record(stream)
+        if backward:
+            for i, rc in enumerate(step.bwd_stages(sp)):
+                assert rc == 0, rc
+                if record:
+                    evs[2 + i].record(stream)
+        return evs
+
+    for _ in range(warmup):
+        one(False)
+    torch.cuda.synchronize()
+    all_evs = []
+    for _ in range(steps):
+        flush.zero_()
+        all_evs.append(one(True))
+    torch.cuda.synchronize()
+    for evs in all_evs:
+        for i, name in enumerate(list(times)):
+            times[name].append(evs[i].elapsed_time(evs[i + 1]))
+    return times
+
+
+def e2e(fa, step: Step, steps: int, warmup: int):
+    """Same step through the public API with pinned host buffers; H2D of the
+    inputs and D2H of O, LSE, dQ, dK, dV inside the timed region."""
+    w = step.w
+    dev = step.q.device
+    names = ["q", "k", "v", "dout"]
+    host_in = {n: step.host[n].pin_memory() for n in names}
+    dev_in = {n: torch.empty_like(step.q) for n in names}
+    outs = [step.o, step.lse, step.dq, step.dk, step.dv]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    kv = step.kv
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for n in names:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        o, lse = fa.forward(dev_in["q"], dev_in["k"], dev_in["v"], causal=w.causal, scale=w.scale,
+                            kv_len=kv, out=step.o, lse=step.lse)
+        fa.backward(dev_in["q"], dev_in["k"], dev_in["v"], o, dev_in["dout"], lse,
+                    causal=w.causal, scale=w.scale, kv_len=kv, workspace=step.ws, dq=step.dq,
+                    dk=step.dk, dv=step.dv)
+        for h, t in zip(host_out, outs):
+            h.copy_(t, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in names)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    return ms, h2d, d2h
+
+
+def cpu_baseline(w: W.Workload, budget_s: float = 12.0):
+    """Times the fp64 oracle (as it stands) on whole heads of the workload
+    until about `budget_s` seconds of CPU work; returns TFLOP/s."""
+    import numpy as np
+
+    import oracle
+    x = W.make_inputs(w.with_(B=1, H=min(w.H, 4)), 0)
+    f_fwd, f_bwd = flops(w.with_(B=1, H=1))
+    done, t0, heads = 0.0, time.perf_counter(), 0
+    while True:
+        h = heads % x["q"].shape[1]
+        kv = None if x["kv_len"] is None else int(x["kv_len"][0])
+        oracle.head_forward(x["q"][0, h], x["k"][0, h], x["v"][0, h], w.scale, w.causal, kv)
+        done += f_fwd
+        if w.backward:
+            oracle.head_backward(x["q"][0, h], x["k"][0, h], x["v"][0, h], x["dout"][0, h],
+                                 w.scale, w.causal, kv)
+            done += f_bwd
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": done / el / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{heads} whole (b,h) heads of {w.name} (N={w.N}, d={w.d}, "
+                      f"{'fwd+bwd' if w.backward else 'fwd'}), numpy fp64, {el:.1f} s",
+            "seconds": el}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, world, rank, local):
+    import exact_io_aware_11_gb300 as fa
+    from exact_io_aware_11_gb300 import build
+    build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    w = W.WORKLOADS[args.workload]
+    step = Step(fa, w, 0, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    times = time_steps(step, args.steps, args.warmup, flush, backward=w.backward)
+    torch.cuda.synchronize()
+    barrier(world)
+    per_kernel = {k: sum(v) / len(v) for k, v in times.items()}
+    ms_step = sum(per_kernel.values())
+    ms_step = max_over_ranks(world, ms_step)
+    f_fwd, f_bwd = flops(w)
+    step_flops = f_fwd + (f_bwd if w.backward else 0.0)
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0, "device watchdog fired during the bench"
+
+    # dominant kernel: roofline against the dense bf16 tensor peak
+    dom = max(per_kernel, key=per_kernel.get)
+    dom_flops = {"fwd": f_fwd, "bwd_main": f_bwd}.get(dom)
+    peak_tf = pk["bf16_tflops"]
+    roofline = None
+    if dom_flops is not None:
+        ach = dom_flops / (per_kernel[dom] * 1e-3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2),
+                    "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4),
+                    "peak_kind": f"{pk_kind} bf16 dense (burst)", "traffic": None}
+
+    e2e_ms, h2d, d2h = e2e(fa, step, max(3, args.steps // 4), 3) if w.backward else (None, 0, 0)
+    clk = clocks.stop()
+
+    out = {
+        "metric": "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded i.i.d. N(0,1) bf16 Q,K,V,dO)",
+        "config": {"workload": f"{w.name}: {'causal' if w.causal else 'non-causal'} fwd+bwd, "
+                               f"B={w.B} H={w.H} N={w.N} d={w.d}",
+                   "pass": "fwd + bwd (preprocess, main, dQ convert)",
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas x{world} (independent (b,h) problems, no collective)"},
+        "pct_of_bf16_peak": round(value / world / peak_tf, 4),
+        "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
+        "fwd_tflops": round(f_fwd / (per_kernel["fwd"] * 1e-3) / 1e12, 2),
+        "gpu_launches": args.steps * len(per_kernel),
+        "roofline": roofline,
+        "clocks": clk,
+    }
+    if e2e_ms is not None:
+        out["e2e"] = {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 3),
+                      "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": round(e2e_ms, 4)}
+    if args.sweep and rank == 0:
+        out["sweep"] = sweep(fa, dev, flush, pk)
+    if rank == 0 and world == 1:
+        out["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+    return out
+
+
+def sweep(fa, dev, flush, pk):
+    """Fwd and bwd TFLOP/s of every workload (few steps each)."""
+    res = {}
+    for name, w in W.WORKLOADS.items():
+        if name == "gpt2_small":
+            continue
+        st = Step(fa, w, 0, dev)
+        t = time_steps(st, 10, 3, flush, backward=w.backward)
+        f_fwd, f_bwd = flops(w)
+        if w.sparse:
+            f_fwd = 4.0 * w.B * w.H * w.d * 128 * 128 * int(st.host["block_mask"].sum())
+        r = {"fwd_ms": round(statistics.median(t["fwd"]), 4),
+             "fwd_tflops": round(f_fwd / (statistics.median(t["fwd"]) * 1e-3) / 1e12, 2)}
+        r["fwd_pct_peak"] = round(r["fwd_tflops"] / pk["bf16_tflops"], 4)
+        if w.backward:
+            mb = statistics.median([a + b + c for a, b, c in zip(t["bwd_pre"], t["bwd_main"],
+                                                                   t["dq_convert"])])
+            r["bwd_ms"] = round(mb, 4)
+            r["bwd_tflops"] = round(f_bwd / (mb * 1e-3) / 1e12, 2)
+            r["bwd_pct_peak"] = round(r["bwd_tflops"] / pk["bf16_tflops"], 4)
+            r["bwd_main_ms"] = round(statistics.median(t["bwd_main"]), 4)
+        res[name] = r
+        del st
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_reference(args, world, rank):
+    """The CPU fp64 oracle, timed on the host cores as it stands."""
+    if rank != 0:
+        return None
+    w = W.WORKLOADS[args.workload]
+    budget = max(2.0, min(20.0, 60.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(w, budget)
+        if i >= args.warmup:
+            vals.append(r)
+    value = statistics.mean(v["value"] for v in vals)
+    secs = sum(v["seconds"] for v in vals)
+    return {
+        "impl": "reference",
+        "metric": "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": secs / len(vals) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {'causal' if w.causal else 'non-causal'} fwd+bwd, "
+                               f"B={w.B} H={w.H} N={w.N} d={w.d}",
+                   "sample": "each step is a bounded sample of whole heads"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": vals[-1]["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt2_small", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+    else:
+        out = run_ours(args, world, rank, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

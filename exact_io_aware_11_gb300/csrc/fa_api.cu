@@ -144,6 +144,85 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   return launch_fwd(a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+struct BwdPtrs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  void* ws;
+};
+
+// Validates and launches the requested backward stages. Pointers a stage does
+// not use may be NULL; every pointer a stage uses must be non-NULL.
+int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int causal, float scale,
+               const int32_t* kv_len, size_t workspace_bytes, cudaStream_t stream) {
+  int st = check_common(B, H, N, d, scale);
+  if (st != FA_OK) return st;
+  const bool pre = stages & kBwdStagePre, mainst = stages & kBwdStageMain,
+             conv = stages & kBwdStageConvert;
+  if (!p.ws) return FA_ERR_INVALID_ARG;
+  if (pre && (!p.o || !p.dout || !p.lse)) return FA_ERR_INVALID_ARG;
+  if (mainst && (!p.q || !p.k || !p.v || !p.dout || !p.dk || !p.dv)) return FA_ERR_INVALID_ARG;
+  if (conv && !p.dq) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const void* all[] = {p.q, p.k, p.v, p.o, p.dout, p.lse, p.dq, p.dk, p.dv, p.ws};
+  for (const void* x : all)
+    if (x && !aligned16(x)) return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  const BwdWorkspace ws = bwd_workspace_layout(B, H, N, d);
+  if (workspace_bytes < ws.total) return FA_ERR_INVALID_ARG;
+  const size_t tb = tensor_bytes(B, H, N, d, 2), lb = tensor_bytes(B, H, N, 1, 4);
+  const void* ins[] = {p.q, p.k, p.v, p.o, p.dout};
+  void* outs[] = {p.dq, p.dk, p.dv};
+  for (int x = 0; x < 3; ++x) {
+    void* out = outs[x];
+    if (!out) continue;
+    for (const void* in : ins)
+      if (in && overlaps(out, tb, in, tb)) return FA_ERR_INVALID_ARG;
+    if ((p.lse && overlaps(out, tb, p.lse, lb)) || overlaps(out, tb, p.ws, ws.total))
+      return FA_ERR_INVALID_ARG;
+    for (int y = x + 1; y < 3; ++y)
+      if (outs[y] && overlaps(out, tb, outs[y], tb)) return FA_ERR_INVALID_ARG;
+  }
+  for (const void* in : ins)
+    if (in && overlaps(p.ws, ws.total, in, tb)) return FA_ERR_INVALID_ARG;
+  if (p.lse && overlaps(p.ws, ws.total, p.lse, lb)) return FA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  st = current_device_info(&dev);
+  if (st != FA_OK) return st;
+  BwdLaunch a;
+  std::memset(&a, 0, sizeof(a));
+  if (mainst && (!encode_bhnd(&a.tm_q, p.q, B, H, N, d) || !encode_bhnd(&a.tm_k, p.k, B, H, N, d) ||
+                 !encode_bhnd(&a.tm_v, p.v, B, H, N, d) ||
+                 !encode_bhnd(&a.tm_do, p.dout, B, H, N, d)))
+    return FA_ERR_CUDA;
+  uint8_t* wsb = static_cast<uint8_t*>(p.ws);
+  a.o = p.o;
+  a.dout = p.dout;
+  a.lse = p.lse;
+  a.dq = p.dq;
+  a.dk = p.dk;
+  a.dv = p.dv;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.kv_len = kv_len;
+  a.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
+  a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
+  a.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
+  a.status = dev.status;
+  a.wait_limit = kWaitLimitCycles;
+  return launch_bwd(a, stages, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
@@ -192,59 +271,28 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
            float scale, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
            struct CUstream_st* stream) {
-  int st = check_common(B, H, N, d, scale);
-  if (st != FA_OK) return st;
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
-    return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  const void* all[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
-  for (const void* p : all)
-    if (!aligned16(p)) return FA_ERR_INVALID_ARG;
-  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
-  const BwdWorkspace ws = bwd_workspace_layout(B, H, N, d);
-  if (workspace_bytes < ws.total) return FA_ERR_INVALID_ARG;
-  const size_t tb = tensor_bytes(B, H, N, d, 2), lb = tensor_bytes(B, H, N, 1, 4);
-  const void* ins[] = {q, k, v, o, dout};
-  void* outs[] = {dq, dk, dv};
-  for (void* out : outs) {
-    for (const void* in : ins)
-      if (overlaps(out, tb, in, tb)) return FA_ERR_INVALID_ARG;
-    if (overlaps(out, tb, lse, lb) || overlaps(out, tb, workspace, ws.total))
-      return FA_ERR_INVALID_ARG;
-  }
-  if (overlaps(dq, tb, dk, tb) || overlaps(dq, tb, dv, tb) || overlaps(dk, tb, dv, tb))
-    return FA_ERR_INVALID_ARG;
-  for (const void* in : ins)
-    if (overlaps(workspace, ws.total, in, tb)) return FA_ERR_INVALID_ARG;
-  if (overlaps(workspace, ws.total, lse, lb)) return FA_ERR_INVALID_ARG;
-  DeviceInfo dev;
-  st = current_device_info(&dev);
-  if (st != FA_OK) return st;
-  BwdLaunch a;
-  std::memset(&a, 0, sizeof(a));
-  if (!encode_bhnd(&a.tm_q, q, B, H, N, d) || !encode_bhnd(&a.tm_k, k, B, H, N, d) ||
-      !encode_bhnd(&a.tm_v, v, B, H, N, d) || !encode_bhnd(&a.tm_do, dout, B, H, N, d))
-    return FA_ERR_CUDA;
-  uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  a.o = o;
-  a.dout = dout;
-  a.lse = lse;
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
-  a.B = B;
-  a.H = H;
-  a.N = N;
-  a.d = d;
-  a.causal = causal;
-  a.scale = scale;
-  a.kv_len = kv_len;
-  a.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
-  a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
-  a.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
-  a.status = dev.status;
-  a.wait_limit = kWaitLimitCycles;
-  return launch_bwd(a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const BwdPtrs p{q, k, v, o, dout, lse, dq, dk, dv, workspace};
+  return bwd_common(kBwdStageAll, p, B, H, N, d, causal, scale, kv_len, workspace_bytes, stream);
+}
+
+int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N,
+                      int d, void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  const BwdPtrs p{nullptr, nullptr, nullptr, o, dout, lse, nullptr, nullptr, nullptr, workspace};
+  return bwd_common(kBwdStagePre, p, B, H, N, d, 0, 1.f, nullptr, workspace_bytes, stream);
+}
+
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                int B, int H, int N, int d, int causal, float scale, const int32_t* kv_len,
+                void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  const BwdPtrs p{q, k, v, nullptr, dout, nullptr, nullptr, dk, dv, workspace};
+  return bwd_common(kBwdStageMain, p, B, H, N, d, causal, scale, kv_len, workspace_bytes, stream);
+}
+
+int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, void* workspace,
+                      size_t workspace_bytes, struct CUstream_st* stream) {
+  const BwdPtrs p{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr,
+                  workspace};
+  return bwd_common(kBwdStageConvert, p, B, H, N, d, 0, 1.f, nullptr, workspace_bytes, stream);
 }
 
 int fa_device_status(void) {

@@ -519,36 +519,45 @@ int grid_for(long long threads) {
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_bwd_t(const BwdLaunch& a, cudaStream_t stream) {
+cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
   using L = BwdLayout<D>;
   const int BH = a.B * a.H;
   const int nt = (a.N + kBlock - 1) / kBlock;
   const int Npad = nt * kBlock;
-  bwd_pre_kernel<D><<<grid_for(static_cast<long long>(BH) * Npad * (D / 8)), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-      a.lse2, a.delta, a.dq_acc, BH, a.N, Npad);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  auto kern = bwd_main_kernel<D, CAUSAL>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-  if (e != cudaSuccess) return e;
-  kern<<<dim3(nt, a.H, a.B), kThreads, L::kSmem, stream>>>(
-      a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc,
-      static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), a.H, a.N, Npad,
-      a.scale, a.kv_len, a.status, a.wait_limit);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  dq_convert_kernel<D><<<grid_for(static_cast<long long>(BH) * a.N * (D / 8)), 256, 0, stream>>>(
-      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), BH, a.N, Npad);
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (stages & kBwdStagePre) {
+    bwd_pre_kernel<D><<<grid_for(static_cast<long long>(BH) * Npad * (D / 8)), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
+        a.lse2, a.delta, a.dq_acc, BH, a.N, Npad);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kBwdStageMain) {
+    auto kern = bwd_main_kernel<D, CAUSAL>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(nt, a.H, a.B), kThreads, L::kSmem, stream>>>(
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc,
+        static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), a.H, a.N, Npad,
+        a.scale, a.kv_len, a.status, a.wait_limit);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kBwdStageConvert) {
+    dq_convert_kernel<D><<<grid_for(static_cast<long long>(BH) * a.N * (D / 8)), 256, 0, stream>>>(
+        a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), BH, a.N, Npad);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdLaunch& a, int stages, cudaStream_t stream) {
   const bool causal = a.causal != 0;
-  if (a.d == 64) return causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
-  return causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+  if (a.d == 64)
+    return causal ? launch_bwd_t<64, true>(a, stages, stream) : launch_bwd_t<64, false>(a, stages, stream);
+  return causal ? launch_bwd_t<128, true>(a, stages, stream) : launch_bwd_t<128, false>(a, stages, stream);
 }
 
 cudaError_t launch_wait_selftest(int* status, long long limit_cycles, cudaStream_t stream) {

@@ -54,7 +54,9 @@ struct BwdWorkspace {
 BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d);
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdLaunch& a, cudaStream_t stream);
+// Backward stages (bit set): preprocess, main kernel, dQ conversion.
+constexpr int kBwdStagePre = 1, kBwdStageMain = 2, kBwdStageConvert = 4, kBwdStageAll = 7;
+cudaError_t launch_bwd(const BwdLaunch& a, int stages, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* status, long long limit_cycles, cudaStream_t stream);
 
 }  // namespace fa

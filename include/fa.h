@@ -93,6 +93,25 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            float scale, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
            struct CUstream_st* stream);
 
+/* The three stages of fa_bwd as separate calls, for callers that schedule
+ * or time them individually. fa_bwd(...) is exactly fa_bwd_preprocess,
+ * fa_bwd_main, fa_bwd_dq_convert on the same stream with the same sizes and
+ * workspace. Arguments mean what they mean for fa_bwd; a stage reads only the
+ * pointers it takes.
+ *   fa_bwd_preprocess: D = rowsum(dO * O), LSE in log2 units, and a zeroed
+ *     fp32 dQ accumulator, all written into the workspace.
+ *   fa_bwd_main: recomputes P tile by tile and writes dK, dV; adds dQ into
+ *     the workspace accumulator. Needs the workspace prepared by
+ *     fa_bwd_preprocess for the same (B, H, N, d) and LSE.
+ *   fa_bwd_dq_convert: dq (bf16) = the workspace accumulator. */
+int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N,
+                      int d, void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk, void* dv,
+                int B, int H, int N, int d, int causal, float scale, const int32_t* kv_len,
+                void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, void* workspace,
+                      size_t workspace_bytes, struct CUstream_st* stream);
+
 /* Block-sparse forward: fa_fwd (non-causal) where query block r attends only
  * to key blocks c with block_mask[r * nb + c] != 0, nb = ceil(N / 128); the
  * masked blocks are -inf and are skipped entirely, so IO and work fall in
