@@ -32,6 +32,7 @@ SIGNATURES = {
     "fa_bwd_main": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, ctypes.c_size_t,
                          _P]),
     "fa_bwd_dq_convert": (_I, [_P, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P]),
     "fa_blocksparse_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P]),
     "fa_device_status": (_I, []),
     "fa_status_string": (ctypes.c_char_p, [_I]),

@@ -112,6 +112,33 @@ int fa_bwd_main(const void* q, const void* k, const void* v, const void* dout, v
 int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, void* workspace,
                       size_t workspace_bytes, struct CUstream_st* stream);
 
+/* Backward pass for callers that cannot allocate device memory. There is no
+ * counterpart of this call in the method's papers: it exists because some
+ * callers of a kernel library may not call cudaMalloc -- a CUDA-graph
+ * capture that must not allocate, a framework that routes every allocation
+ * through its own pool, a plugin that receives tensors but no allocator --
+ * and fa_bwd needs a workspace.
+ *
+ * Same arguments and results as fa_bwd, minus the workspace: the library
+ * uses its own static device buffer of FA_NOALLOC_SCRATCH_BYTES (64 MiB),
+ * which every GPU that loads libfa.so holds until the process exits. The
+ * caller still passes every input and output. Nothing is allocated or freed.
+ *   - Limit: the call returns FA_ERR_INVALID_ARG, without launching, when
+ *     fa_bwd_workspace_bytes(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES (for
+ *     example B*H*Npad <= 254,200 rows at d = 64 and <= 129,055 at d = 128,
+ *     Npad = N rounded up to a multiple of 128).
+ *   - Set-up: the first call on each device, with that device current, looks
+ *     up the buffer's device address (cudaGetSymbolAddress). Make that first
+ *     call before any stream capture on that device.
+ *   - Sharing: all calls on a device share the one buffer, and it keeps the
+ *     last call's contents; each call re-initialises what it reads. Calls
+ *     whose kernels overlap on the GPU (different streams without ordering
+ *     between them) race on the buffer and give wrong results. */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, const int32_t* kv_len, struct CUstream_st* stream);
+
 /* Block-sparse forward: fa_fwd (non-causal) where query block r attends only
  * to key blocks c with block_mask[r * nb + c] != 0, nb = ceil(N / 128); the
  * masked blocks are -inf and are skipped entirely, so IO and work fall in
