@@ -127,7 +127,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   FwdLaunch a;
   std::memset(&a, 0, sizeof(a));
   if (!encode_bhnd(&a.tm_q, q, B, H, N, d) || !encode_bhnd(&a.tm_k, k, B, H, N, d) ||
-      !encode_bhnd(&a.tm_v, v, B, H, N, d))
+      !encode_bhnd(&a.tm_v, v, B, H, N, d) || !encode_bhnd(&a.tm_o, o, B, H, N, d))
     return FA_ERR_CUDA;
   a.o = o;
   a.lse = lse;

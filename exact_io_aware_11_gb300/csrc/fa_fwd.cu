@@ -7,19 +7,31 @@
 // and the N x N matrices S and P are never written to HBM (condensed paper
 // sample_paper.md, section 3 "Tiling" / "Softmax rescaling"; Medium article
 // "No More Quadratic Complexity for Transformers", Figure 1). The pages put
-// K/V in the outer loop; here each CTA owns one 128-row Q tile and streams
-// the K/V tiles past it, which gives the same exact result and keeps the
-// running statistics in registers.
+// K/V in the outer loop; here each CTA keeps two 128-row Q tiles resident and
+// streams the K/V tiles past them, which gives the same exact result, keeps
+// the running statistics in registers and loads every K/V tile once for two
+// Q tiles.
 //
-// One CTA = one 128-row Q tile of one (batch, head); 6 warps:
-//   warp 4      TMA producer: Q once, then K_j / V_j into a 2-stage ring
-//   warp 5      MMA issuer:   S_j = Q K_j^T into TMEM (double-buffered),
-//                             O += P_j V_j into a TMEM accumulator
-//   warps 0-3   softmax:      thread t owns query row t (= TMEM lane t):
-//                             masks, running max m / sum l, P_j = exp2(.) in
-//                             bf16 to shared memory, O rescale in TMEM,
-//                             epilogue O / l and LSE = (m + log2 l) ln 2.
-// TMEM columns: [0,128) S buffer 0, [128,256) S buffer 1, [256,256+d) O.
+// One CTA = Q tiles A and B of one (batch, head); 10 warps:
+//   warps 0-3   softmax of tile A: thread t owns query row t (= TMEM lane t)
+//   warps 4-7   softmax of tile B
+//   warp 8      TMA producer: Q_A, Q_B once; K_j, V_j through separate rings
+//   warp 9      MMA issuer, in the order
+//                 S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+//               so that the tensor core computes one tile's MMAs while the
+//               other tile's softmax runs.
+// TMEM columns: S_A [0,128), S_B [128,256) (fp32). After reading S_t the
+// softmax writes P_t in bf16 over the first 64 columns of S_t and the PV MMA
+// takes it from there as its A operand, so P never touches shared memory.
+// O_A [256, 256+d), O_B [256+d, 256+2d): fp32 accumulators.
+//
+// Rescaling is lazy: a row's reference maximum m only moves when the new
+// tile's maximum exceeds it by more than 8 (log2 units), so P <= 2^8 and O is
+// rescaled in TMEM only on those rare tiles; the final O / l is exact because
+// O and l always share the same m.
+//
+// Causal: CTA x pairs Q tiles x and nqt-1-x, so every CTA does the same
+// number of K/V tiles. Otherwise tiles 2x and 2x+1 are paired.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -28,22 +40,24 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
+constexpr int kThreads = 320;
 constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled chunk (64 bf16 cols)
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 
 template <int D>
 struct FwdLayout {
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kChunks * kChunk;  // one 128 x D bf16 tile
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTile;
-  static constexpr int kV = kK + kStages * kTile;
-  static constexpr int kP = kV + kStages * kTile;
-  static constexpr int kBar = kP + 2 * kChunk;  // P: 128 rows x 128 keys bf16
+  static constexpr int kKS = 3;                   // K ring slots
+  static constexpr int kVS = (D == 128) ? 2 : 3;  // V ring slots
+  static constexpr int kQ = 0;                    // Q_A, Q_B (reused to stage O)
+  static constexpr int kK = kQ + 2 * kTile;
+  static constexpr int kV = kK + kKS * kTile;
+  static constexpr int kBar = kV + kVS * kTile;
   static constexpr int kEnd = kBar + 256;
   static constexpr int kSmem = kEnd + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t kTO = 256;       // O_A; O_B at kTO + D
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -51,60 +65,119 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return p + ((1024u - (a & 1023u)) & 1023u);
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Which K/V tiles a Q tile visits: j < end, and the block-mask bit if any.
+struct TileSet {
+  int end;
+  const uint8_t* mrow;
+  __device__ bool has(int j) const { return j < end && (mrow == nullptr || mrow[j] != 0); }
+};
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                float* __restrict__ lse_out, int H, int N, float scale_log2,
                const int32_t* __restrict__ kv_len, const uint8_t* __restrict__ block_mask,
                int* status, long long wait_limit) {
   using L = FwdLayout<D>;
+  constexpr int KS = L::kKS, VS = L::kVS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* bar_q = bars + 0;
-  uint64_t* bar_kfull = bars + 1;    // [2]
-  uint64_t* bar_vfull = bars + 3;    // [2]
-  uint64_t* bar_kvempty = bars + 5;  // [2]
-  uint64_t* bar_sfull = bars + 7;    // [2]
-  uint64_t* bar_pfull = bars + 9;
-  uint64_t* bar_odone = bars + 10;
-  uint64_t* bar_final = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-  int* abort_flag = reinterpret_cast<int*>(bars + 13);
+  uint64_t* bar_kfull = bars + 1;    // [KS]
+  uint64_t* bar_kempty = bars + 4;   // [KS]
+  uint64_t* bar_vfull = bars + 7;    // [VS]
+  uint64_t* bar_vempty = bars + 10;  // [VS]
+  uint64_t* bar_sfull = bars + 13;   // [2]
+  uint64_t* bar_pfull = bars + 15;   // [2]
+  uint64_t* bar_odone = bars + 17;   // [2]
+  uint64_t* bar_final = bars + 19;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  int* abort_flag = reinterpret_cast<int*>(bars + 21);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nqt = (N + kBlock - 1) / kBlock;
-  // Causal: heaviest tiles first so the tail of the grid is short.
-  const int qt = CAUSAL ? (nqt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
   const int bh = blockIdx.z * H + blockIdx.y;
+  int qtile[2];
+  if (CAUSAL) {
+    qtile[0] = blockIdx.x;
+    qtile[1] = nqt - 1 - static_cast<int>(blockIdx.x);
+    if (qtile[1] == qtile[0]) qtile[1] = -1;
+  } else {
+    qtile[0] = 2 * blockIdx.x;
+    qtile[1] = 2 * blockIdx.x + 1 < nqt ? 2 * blockIdx.x + 1 : -1;
+  }
   int kv_bound = N;
   if (kv_len != nullptr) kv_bound = min(N, max(0, kv_len[blockIdx.z]));
-  int jend = (kv_bound + kBlock - 1) / kBlock;
-  if (CAUSAL) jend = min(jend, qt + 1);
-  const uint8_t* mrow = block_mask ? block_mask + static_cast<size_t>(qt) * nqt : nullptr;
-  auto next_tile = [&](int j) {
-    if (mrow != nullptr)
-      while (j < jend && mrow[j] == 0) ++j;
+  const int kv_tiles = (kv_bound + kBlock - 1) / kBlock;
+  TileSet ts[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = qtile[t];
+    ts[t].end = qt < 0 ? 0 : (CAUSAL ? min(kv_tiles, qt + 1) : kv_tiles);
+    ts[t].mrow = (block_mask != nullptr && qt >= 0) ? block_mask + static_cast<size_t>(qt) * nqt
+                                                    : nullptr;
+  }
+  const int uend = max(ts[0].end, ts[1].end);
+  auto next_union = [&](int j) {
+    while (j < uend && !ts[0].has(j) && !ts[1].has(j)) ++j;
     return j;
   };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(bar_kfull + s, 1);
-      mbar_init(bar_vfull + s, 1);
-      mbar_init(bar_kvempty + s, 1);
-      mbar_init(bar_sfull + s, 1);
+      mbar_init(bar_kempty + s, 1);
     }
-    mbar_init(bar_pfull, 4);
-    mbar_init(bar_odone, 1);
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(bar_vfull + s, 1);
+      mbar_init(bar_vempty + s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_sfull + t, 1);
+      mbar_init(bar_pfull + t, 4);
+      mbar_init(bar_odone + t, 1);
+    }
     mbar_init(bar_final, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -114,98 +187,123 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{wait_limit, status, abort_flag};
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    int k_issued = 0, v_issued = 0;
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_expect_tx(bar_q, L::kTile);
-      for (int c = 0; c < L::kChunks; ++c)
-        tma_load_3d(smem + L::kQ + c * kChunk, &tm_q, bar_q, c * 64, qt * kBlock, bh);
+      tma_prefetch_desc(&tm_o);
+      mbar_expect_tx(bar_q, (qtile[1] >= 0 ? 2 : 1) * L::kTile);
+      for (int t = 0; t < 2; ++t)
+        if (qtile[t] >= 0)
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kQ + t * L::kTile + c * kChunk, &tm_q, bar_q, c * 64,
+                        qtile[t] * kBlock, bh);
     }
-    int issued = 0;
-    int jj = 0;
-    for (int j = next_tile(0); j < jend; j = next_tile(j + 1), ++jj) {
-      const int s = jj & 1;
-      if (jj >= kStages && !mbar_wait_warp(bar_kvempty + s, ((jj >> 1) - 1) & 1, wd)) break;
+    int u = 0;
+    for (int j = next_union(0); j < uend; j = next_union(j + 1), ++u) {
+      const int ks = u % KS, vs = u % VS;
+      if (u >= KS && !mbar_wait_warp(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) break;
       if (lane == 0) {
-        mbar_expect_tx(bar_kfull + s, L::kTile);
+        mbar_expect_tx(bar_kfull + ks, L::kTile);
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(smem + L::kK + s * L::kTile + c * kChunk, &tm_k, bar_kfull + s, c * 64,
-                      j * kBlock, bh);
-        mbar_expect_tx(bar_vfull + s, L::kTile);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(smem + L::kV + s * L::kTile + c * kChunk, &tm_v, bar_vfull + s, c * 64,
+          tma_load_3d(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
                       j * kBlock, bh);
       }
       __syncwarp();
-      issued = jj + 1;
+      k_issued = u + 1;
+      if (u >= VS && !mbar_wait_warp(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) break;
+      if (lane == 0) {
+        mbar_expect_tx(bar_vfull + vs, L::kTile);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
+                      j * kBlock, bh);
+      }
+      __syncwarp();
+      v_issued = u + 1;
     }
-    // Let every copy already in flight land before the CTA can exit.
+    // Let every copy in flight land before the CTA can exit (bounded).
     if (lane == 0) {
       mbar_wait_drain(bar_q, 0, wait_limit);
-      for (int t = max(0, issued - kStages); t < issued; ++t) {
-        mbar_wait_drain(bar_kfull + (t & 1), (t >> 1) & 1, wait_limit);
-        mbar_wait_drain(bar_vfull + (t & 1), (t >> 1) & 1, wait_limit);
-      }
+      for (int t = max(0, k_issued - KS); t < k_issued; ++t)
+        mbar_wait_drain(bar_kfull + (t % KS), (t / KS) & 1, wait_limit);
+      for (int t = max(0, v_issued - VS); t < v_issued; ++t)
+        mbar_wait_drain(bar_vfull + (t % VS), (t / VS) & 1, wait_limit);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
-    constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P K-major, V MN-major
+    constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
     const uint32_t q_base = smem_u32(smem + L::kQ);
     const uint32_t k_base = smem_u32(smem + L::kK);
     const uint32_t v_base = smem_u32(smem + L::kV);
-    const uint32_t p_base = smem_u32(smem + L::kP);
-    auto issue_pv = [&](int t) -> bool {
-      if (!mbar_wait_warp(bar_pfull, t & 1, wd)) return false;
-      if (!mbar_wait_warp(bar_vfull + (t & 1), (t >> 1) & 1, wd)) return false;
+    int n_s[2] = {0, 0}, n_pv[2] = {0, 0};
+    bool ok = mbar_wait_warp(bar_q, 0, wd);
+    auto issue_s = [&](int t, int u) -> bool {
+      if (!mbar_wait_warp(bar_kfull + (u % KS), (u / KS) & 1, wd)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t vb = v_base + (t & 1) * L::kTile;
+        const uint32_t qb = q_base + t * L::kTile;
+        const uint32_t kb = k_base + (u % KS) * L::kTile;
 #pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk) {
-          // A = P (128 x 16 slice of keys), B = V (16 keys x D), MN-major.
-          const uint64_t a = sdesc_sw128(p_base + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(vb + kk * 2048, kChunk, 1024);
-          mma_ss(tmem + 256, a, b, kIdO, (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+          mma_ss(tmem + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                 kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_kvempty + (t & 1));
-        mma_commit(bar_odone);
+        mma_commit(bar_sfull + t);
       }
       __syncwarp();
+      ++n_s[t];
       return true;
     };
-    bool ok = mbar_wait_warp(bar_q, 0, wd);
-    int jj = 0;
+    auto issue_pv = [&](int t, int u) -> bool {
+      if (!mbar_wait_warp(bar_pfull + t, n_pv[t] & 1, wd)) return false;
+      if (!mbar_wait_warp(bar_vfull + (u % VS), (u / VS) & 1, wd)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t vb = v_base + (u % VS) * L::kTile;
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk) {
+          // A = P (bf16 pairs in the first 64 columns of S_t), B = V, MN-major.
+          mma_ts(tmem + L::kTO + t * D, tmem + t * 128 + kk * 8,
+                 sdesc_sw128(vb + kk * 2048, kChunk, 1024), kIdO,
+                 (n_pv[t] > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar_odone + t);
+      }
+      __syncwarp();
+      ++n_pv[t];
+      return true;
+    };
     if (ok) {
       tc_fence_after();
-      for (int j = next_tile(0); j < jend; j = next_tile(j + 1), ++jj) {
-        const int s = jj & 1;
-        if (!mbar_wait_warp(bar_kfull + s, (jj >> 1) & 1, wd)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t kb = k_base + s * L::kTile;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-            mma_ss(tmem + s * 128, sdesc_sw128(q_base + off, 16, 1024),
-                   sdesc_sw128(kb + off, 16, 1024), kIdS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar_sfull + s);
-        }
+      int u = 0;
+      int j = next_union(0);
+      if (j < uend) {
+        for (int t = 0; t < 2 && ok; ++t)
+          if (ts[t].has(j)) ok = issue_s(t, 0);
+        if (ok && lane == 0) mma_commit(bar_kempty + 0);
         __syncwarp();
-        if (jj >= 1 && !issue_pv(jj - 1)) {
-          ok = false;
-          break;
-        }
       }
-      if (ok && jj >= 1) issue_pv(jj - 1);
+      while (ok && j < uend) {
+        const int jn = next_union(j + 1);
+        const int un = u + 1;
+        // tile A: P_A(j) V_j, then S_A(j+1) over the columns P_A(j) just left
+        if (ts[0].has(j)) ok = issue_pv(0, u);
+        if (ok && jn < uend && ts[0].has(jn)) ok = issue_s(0, un);
+        if (ok && ts[1].has(j)) ok = issue_pv(1, u);
+        if (ok && lane == 0) mma_commit(bar_vempty + (u % VS));
+        __syncwarp();
+        if (ok && jn < uend && ts[1].has(jn)) ok = issue_s(1, un);
+        if (ok && jn < uend && lane == 0) mma_commit(bar_kempty + (un % KS));
+        __syncwarp();
+        j = jn;
+        u = un;
+      }
     }
     if (lane == 0) {
       mma_commit(bar_final);
@@ -213,134 +311,147 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    const int t = threadIdx.x;  // row within the tile == TMEM lane
-    const int row = qt * kBlock + t;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t p_base = smem_u32(smem + L::kP);
-    float m = -INFINITY;  // running max of scale*log2(e)*s
-    float l = 0.f;        // running sum of exp2(scale*log2(e)*s - m)
-    bool ok = true;
-    int jj = 0;
-    for (int j = next_tile(0); j < jend; j = next_tile(j + 1), ++jj) {
-      const int s = jj & 1;
-      if (!mbar_wait_warp(bar_sfull + s, (jj >> 1) & 1, wd)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s * 128 + c * 32, r[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence(r[c]);
-      float sv[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(r[c >> 5][c & 31]);
-      const bool edge = (j + 1) * kBlock > kv_bound || (CAUSAL && j == qt);
-      if (edge) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int key = j * kBlock + c;
-          if (key >= kv_bound || (CAUSAL && key > row)) sv[c] = -INFINITY;
-        }
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = sv[i];
-#pragma unroll
-      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
-      const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m, tile_max * scale_log2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m - m_use);
-      uint32_t pk[64];
-      float ps[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ps[i] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2(fmaf(sv[2 * c], scale_log2, -m_use));
-        const float p1 = ex2(fmaf(sv[2 * c + 1], scale_log2, -m_use));
-        pk[c] = pack_bf16(p0, p1);
-        ps[c & 7] += p0 + p1;
-      }
-      const float tile_sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      // P_{jj-1} V must be done before P is overwritten and O is rescaled.
-      if (jj >= 1) {
-        if (!mbar_wait_warp(bar_odone, (jj - 1) & 1, wd)) {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int t = warp >> 2;              // which Q tile
+    const int r = threadIdx.x & 127;      // row within the tile == TMEM lane
+    const int qt = qtile[t];
+    if (qt >= 0) {
+      const int row = qt * kBlock + r;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+      const uint32_t s_col = t * 128;
+      const uint32_t o_col = L::kTO + t * D;
+      const TileSet my = ts[t];
+      float m = -INFINITY;  // reference max, log2 units (scale folded in)
+      float l = 0.f;        // sum of exp2(s * scale_log2 - m) over visited keys
+      bool ok = true;
+      int n = 0;
+      for (int j = 0; j < my.end; ++j) {
+        if (!my.has(j)) continue;
+        if (!mbar_wait_warp(bar_sfull + t, n & 1, wd)) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      // P -> shared memory, K-major with the 128-byte swizzle the MMA expects:
-      // row t, 16-byte unit u of chunk (u / 8) lands at unit (u % 8) ^ (t % 8).
+        uint32_t rs[4][32];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const uint32_t addr =
-            p_base + (u >> 3) * kChunk + t * 128 + ((((u & 7) ^ (t & 7))) << 4);
-        st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      }
-      if (jj >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, rs[c]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c0 = 0; c0 < D / 32; ++c0) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + 256 + c0 * 32, o);
-          tmem_wait_ld();
-          reg_fence(o);
+        for (int c = 0; c < 4; ++c) reg_fence(rs[c]);
+        float sv[128];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(lane_base + 256 + c0 * 32, o);
+        for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(rs[c >> 5][c & 31]);
+        if ((j + 1) * kBlock > kv_bound || (CAUSAL && j == qt)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int key = j * kBlock + c;
+            if (key >= kv_bound || (CAUSAL && key > row)) sv[c] = -INFINITY;
+          }
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = max3(sv[i], sv[i + 8], sv[i + 16]);
+#pragma unroll
+        for (int c = 24; c < 128; c += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mx[i] = (c + 8 + i < 128) ? max3(mx[i], sv[c + i], sv[c + 8 + i]) : fmaxf(mx[i], sv[c + i]);
+        }
+        const float tmax =
+            max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+            scale_log2;
+        const bool grow = tmax > m + kRescaleThreshold;
+        const float m_new = grow ? tmax : m;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = grow ? ex2(m - m_use) : 1.f;
+        uint32_t pk[64];
+        float ps[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ps[i] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2(fmaf(sv[2 * c], scale_log2, -m_use));
+          const float p1 = ex2(fmaf(sv[2 * c + 1], scale_log2, -m_use));
+          pk[c] = pack_bf16(p0, p1);
+          ps[c & 7] += p0 + p1;
+        }
+        const float tsum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        // P_t over the first 64 columns of S_t (its fp32 values are already in registers)
+        tmem_st32(lane_base + s_col, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st32(lane_base + s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        if (n >= 1 && __any_sync(0xffffffffu, grow)) {
+          // O must be quiescent (P_t(n-1) V done) before it is rescaled.
+          if (!mbar_wait_warp(bar_odone + t, (n - 1) & 1, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D / 32; ++c0) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + o_col + c0 * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(lane_base + o_col + c0 * 32, o);
+          }
         }
         tmem_wait_st();
+        l = l * alpha + tsum;
+        m = m_new;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pfull + t);
+        ++n;
       }
-      l = l * alpha + tile_sum;
-      m = m_new;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pfull);
-    }
-    // ------------------------------------------------------------ epilogue
-    bool have = ok && jj > 0;
-    if (have) have = mbar_wait_warp(bar_odone, (jj - 1) & 1, wd);
-    if (have) tc_fence_after();
-    const bool live = have && l > 0.f;
-    const float inv = live ? 1.f / l : 0.f;
-    const bool row_ok = row < N;
-    uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * N + row) * D);
+      // ---------------------------------------------------------- epilogue
+      bool have = ok && n > 0;
+      if (have) have = mbar_wait_warp(bar_odone + t, (n - 1) & 1, wd);
+      if (have) tc_fence_after();
+      const bool live = have && l > 0.f;
+      const float inv = live ? 1.f / l : 0.f;
+      // O row -> the Q_t buffer (free now), same 128-byte swizzled layout as Q,
+      // then one TMA store per 64-column chunk (rows >= N are clipped).
+      uint8_t* stage = smem + L::kQ + t * L::kTile;
+      const uint32_t st_base = smem_u32(stage);
 #pragma unroll
-    for (int c0 = 0; c0 < D / 32; ++c0) {
-      uint32_t o[32];
-      if (have) {
-        tmem_ld32(lane_base + 256 + c0 * 32, o);
-        tmem_wait_ld();
-        reg_fence(o);
-      } else {
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t o[32];
+        if (have) {
+          tmem_ld32(lane_base + o_col + c0 * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
-      }
-      if (row_ok) {
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          uint4 w;
-          w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-          w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-          w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-          w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-          orow[c0 * 4 + v] = w;
+          const int unit = c0 * 4 + v;  // 16-byte unit of the row (8 columns)
+          const uint32_t addr = st_base + (unit >> 3) * kChunk + r * 128 + (((unit & 7) ^ (r & 7)) << 4);
+          st_shared_v4(addr,
+                       pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                       pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                       pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                       pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
         }
       }
+      if (row < N)
+        lse_out[static_cast<size_t>(bh) * N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, 128);
+      if (r == 0) {
+        for (int c = 0; c < L::kChunks; ++c) tma_store_3d(&tm_o, stage + c * kChunk, c * 64, qt * kBlock, bh);
+        bulk_commit();
+        bulk_wait_read0();
+      }
     }
-    if (row_ok) lse_out[static_cast<size_t>(bh) * N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -353,10 +464,9 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   const int nqt = (a.N + kBlock - 1) / kBlock;
-  const dim3 grid(nqt, a.H, a.B);
+  const dim3 grid((nqt + 1) / 2, a.H, a.B);
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, L::kSmem, stream>>>(a.tm_q, a.tm_k, a.tm_v,
-                                             static_cast<__nv_bfloat16*>(a.o), a.lse, a.H, a.N,
+  kern<<<grid, kThreads, L::kSmem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.H, a.N,
                                              scale_log2, a.kv_len, a.block_mask, a.status,
                                              a.wait_limit);
   return cudaGetLastError();

@@ -16,7 +16,7 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 constexpr int kBlock = 128;
 
 struct FwdLaunch {
-  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H, N, d], box 64 x 128 x 1, 128B swizzle
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H, N, d], box 64 x 128 x 1, 128B swizzle
   void* o;
   float* lse;
   int B, H, N, d;
