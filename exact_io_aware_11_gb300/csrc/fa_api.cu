@@ -93,6 +93,22 @@ bool encode_bhnd(CUtensorMap* map, const void* base, int B, int H, int N, int d)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [B*H, rows, d] as a 3-D tensor map; box = 32 columns (128 bytes) x 128
+// rows x 1 head, 128-byte swizzle (the backward's dQ accumulator).
+bool encode_f32_rows(CUtensorMap* map, const void* base, int BH, int rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d) * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kBlock), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int check_common(int B, int H, int N, int d, float scale) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
@@ -197,11 +213,15 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
   if (st != FA_OK) return st;
   BwdLaunch a;
   std::memset(&a, 0, sizeof(a));
+  uint8_t* wsb = static_cast<uint8_t*>(p.ws);
+  const int npad = (N + kBlock - 1) / kBlock * kBlock;
   if (mainst && (!encode_bhnd(&a.tm_q, p.q, B, H, N, d) || !encode_bhnd(&a.tm_k, p.k, B, H, N, d) ||
                  !encode_bhnd(&a.tm_v, p.v, B, H, N, d) ||
-                 !encode_bhnd(&a.tm_do, p.dout, B, H, N, d)))
+                 !encode_bhnd(&a.tm_do, p.dout, B, H, N, d) ||
+                 !encode_bhnd(&a.tm_dk, p.dk, B, H, N, d) ||
+                 !encode_bhnd(&a.tm_dv, p.dv, B, H, N, d) ||
+                 !encode_f32_rows(&a.tm_dqacc, wsb + ws.dq_off, B * H, npad, d)))
     return FA_ERR_CUDA;
-  uint8_t* wsb = static_cast<uint8_t*>(p.ws);
   a.o = p.o;
   a.dout = p.dout;
   a.lse = p.lse;

@@ -11,20 +11,24 @@
 //
 // 1. bwd_pre_kernel   D = rowsum(dO * O), LSE * log2(e), zero the fp32 dQ
 //                     accumulator (bandwidth-bound, 16-byte accesses).
-// 2. bwd_main_kernel  one CTA per 128-key tile of one (batch, head); it keeps
-//                     K_j, V_j in shared memory and dK_j, dV_j in TMEM and
-//                     loops over the Q tiles:
-//                       S^T  = K_j Q_i^T        (TMEM, key rows on lanes)
-//                       dP^T = V_j dO_i^T       (TMEM)
-//                       P^T  = exp2(S^T * scale*log2e - LSE2_i)  -> smem bf16
+// 2. bwd_main_kernel  one CTA per 128-key tile j of one (batch, head); K_j and
+//                     V_j stay in shared memory, dK_j and dV_j accumulate in
+//                     TMEM, and the CTA loops over the Q tiles i:
+//                       S^T  = K_j Q_i^T    TMEM, key rows on lanes
+//                       dP^T = V_j dO_i^T   TMEM
+//                       P^T  = exp2(S^T * scale*log2e - LSE2_i), bf16, written
+//                              back into the S^T columns and used from TMEM
 //                       dV_j += P^T dO_i
-//                       dS^T = P^T * (dP^T - D_i)                -> smem bf16
+//                       dS^T = P^T * (dP^T - D_i), bf16 -> shared memory
 //                       dK_j += dS^T Q_i
-//                       dQ_i  = dS K_j          (TMEM) -> fp32 atomics into the
-//                                                        workspace, times scale
-//                     warps 0-3 compute P / dS (thread t = key t = TMEM lane t),
-//                     warp 4 issues TMA, warp 5 issues tcgen05.mma, warps 6-9
-//                     drain dQ (thread = query row).
+//                       dQ_i  = dS K_j      TMEM -> shared memory (fp32) -> one
+//                              TMA bulk reduce-add per 32-column chunk into the
+//                              fp32 workspace accumulator
+//                     Warps 0-7 compute P and dS (warps w and w+4 share the
+//                     key rows of TMEM lane quarter w % 4 and split the 128
+//                     query columns), warp 8 issues TMA, warp 9 issues
+//                     tcgen05.mma, warps 10-13 drain dQ. S^T of tile i+1 is
+//                     computed while dS of tile i is being formed.
 // 3. dq_convert_kernel  dQ bf16 = fp32 accumulator.
 #include <cuda_bf16.h>
 
@@ -34,33 +38,69 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr int kChunk = 128 * 128;  // one 128-row x 128-byte swizzled chunk
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdLayout {
   static constexpr int kChunks = D / 64;
-  static constexpr int kTile = kChunks * kChunk;
-  static constexpr int kStages = (D == 64) ? 2 : 1;  // Q / dO / LSE2 / D stages
+  static constexpr int kTile = kChunks * kChunk;     // 128 x D bf16
+  static constexpr int kQS = 2;                      // Q (+ LSE2 / D) stages
+  static constexpr int kDS = (D == 64) ? 2 : 1;      // dO stages
+  static constexpr int kDQChunks = (D == 64) ? 2 : 1;  // 128 x 32 fp32 chunks staged at once
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTile;
   static constexpr int kQ = kV + kTile;
-  static constexpr int kDO = kQ + kStages * kTile;
-  static constexpr int kStat = kDO + kStages * kTile;  // per stage: lse2[128], delta[128]
-  static constexpr int kP = kStat + kStages * 1024;
-  static constexpr int kDS = kP + 2 * kChunk;
-  static constexpr int kBar = kDS + 2 * kChunk;
+  static constexpr int kDO = kQ + kQS * kTile;
+  static constexpr int kStat = kDO + kDS * kTile;    // per Q stage: lse2[128], delta[128]
+  static constexpr int kDSb = kStat + kQS * 1024;    // dS^T, bf16, 2 chunks
+  static constexpr int kDQ = kDSb + 2 * kChunk;      // dQ staging (fp32, 128-byte swizzle)
+  static constexpr int kBar = kDQ + kDQChunks * kChunk;
   static constexpr int kEnd = kBar + 256;
   static constexpr int kSmem = kEnd + 1024;
   // TMEM columns
   static constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256, kTDK = 256 + D;
-  static constexpr uint32_t kTDQ = (D == 64) ? 384 : 0;  // d=128: dQ reuses the S^T columns
+  static constexpr uint32_t kTDQ = (D == 64) ? 384 : 128;  // d=128: dQ reuses the dP^T columns
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t a = smem_u32(p);
   return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
+                                                  int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ----------------------------------------------------------------- preprocess
@@ -148,29 +188,31 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const float* __restrict__ lse2, const float* __restrict__ delta,
-                    float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
-                    __nv_bfloat16* __restrict__ dv, int H, int N, int Npad, float scale,
-                    const int32_t* __restrict__ kv_len, int* status, long long wait_limit) {
+                    const __grid_constant__ CUtensorMap tm_dqacc,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                    const float* __restrict__ lse2, const float* __restrict__ delta, int H, int N,
+                    int Npad, float scale, const int32_t* __restrict__ kv_len, int* status,
+                    long long wait_limit) {
   using L = BwdLayout<D>;
-  constexpr int S = L::kStages;
+  constexpr int QS = L::kQS, DS = L::kDS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* bar_kv = bars + 0;
-  uint64_t* bar_qfull = bars + 1;   // [S]
-  uint64_t* bar_qempty = bars + 3;  // [S]
-  uint64_t* bar_sfull = bars + 5;
-  uint64_t* bar_dpfull = bars + 6;
-  uint64_t* bar_pready = bars + 7;
-  uint64_t* bar_pfree = bars + 8;
-  uint64_t* bar_dsready = bars + 9;
-  uint64_t* bar_dsfree = bars + 10;
-  uint64_t* bar_dqfull = bars + 11;
-  uint64_t* bar_dqfree = bars + 12;
-  uint64_t* bar_final = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
-  int* abort_flag = reinterpret_cast<int*>(bars + 15);
+  uint64_t* bar_qfull = bars + 1;    // [QS]
+  uint64_t* bar_qempty = bars + 3;   // [QS]
+  uint64_t* bar_dofull = bars + 5;   // [DS]
+  uint64_t* bar_doempty = bars + 7;  // [DS]
+  uint64_t* bar_sfull = bars + 9;
+  uint64_t* bar_dpfull = bars + 10;
+  uint64_t* bar_pready = bars + 11;
+  uint64_t* bar_dsready = bars + 12;
+  uint64_t* bar_dsfree = bars + 13;
+  uint64_t* bar_dqfull = bars + 14;
+  uint64_t* bar_dqfree = bars + 15;
+  uint64_t* bar_final = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  int* abort_flag = reinterpret_cast<int*>(bars + 18);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -186,15 +228,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < QS; ++s) {
       mbar_init(bar_qfull + s, 1);
       mbar_init(bar_qempty + s, 1);
     }
+    for (int s = 0; s < DS; ++s) {
+      mbar_init(bar_dofull + s, 1);
+      mbar_init(bar_doempty + s, 1);
+    }
     mbar_init(bar_sfull, 1);
     mbar_init(bar_dpfull, 1);
-    mbar_init(bar_pready, 4);
-    mbar_init(bar_pfree, 1);
-    mbar_init(bar_dsready, 4);
+    mbar_init(bar_pready, 8);
+    mbar_init(bar_dsready, 8);
     mbar_init(bar_dsfree, 1);
     mbar_init(bar_dqfull, 1);
     mbar_init(bar_dqfree, 4);
@@ -202,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -212,15 +257,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{wait_limit, status, abort_flag};
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    int issued = 0;
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    int q_issued = 0, do_issued = 0;
     if (n_iter > 0) {
       if (lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dqacc);
         mbar_expect_tx(bar_kv, 2 * L::kTile);
         for (int c = 0; c < L::kChunks; ++c) {
           tma_load_3d(smem + L::kK + c * kChunk, &tm_k, bar_kv, c * 64, j * kBlock, bh);
@@ -228,80 +274,103 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int it = 0; it < n_iter; ++it) {
-        const int s = it % S;
-        const int i = i0 + it;
-        if (it >= S && !mbar_wait_warp(bar_qempty + s, ((it / S) - 1) & 1, wd)) break;
+        const int i = i0 + it, qs = it % QS, ds = it % DS;
+        if (it >= QS && !mbar_wait_warp(bar_qempty + qs, ((it / QS) - 1) & 1, wd)) break;
         if (lane == 0) {
-          mbar_expect_tx(bar_qfull + s, 2 * L::kTile + 1024);
-          for (int c = 0; c < L::kChunks; ++c) {
-            tma_load_3d(smem + L::kQ + s * L::kTile + c * kChunk, &tm_q, bar_qfull + s, c * 64,
+          mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
                         i * kBlock, bh);
-            tma_load_3d(smem + L::kDO + s * L::kTile + c * kChunk, &tm_do, bar_qfull + s, c * 64,
-                        i * kBlock, bh);
-          }
           const size_t roff = static_cast<size_t>(bh) * Npad + static_cast<size_t>(i) * kBlock;
-          bulk_load(smem + L::kStat + s * 1024, lse2 + roff, 512, bar_qfull + s);
-          bulk_load(smem + L::kStat + s * 1024 + 512, delta + roff, 512, bar_qfull + s);
+          bulk_load(smem + L::kStat + qs * 1024, lse2 + roff, 512, bar_qfull + qs);
+          bulk_load(smem + L::kStat + qs * 1024 + 512, delta + roff, 512, bar_qfull + qs);
         }
         __syncwarp();
-        issued = it + 1;
+        q_issued = it + 1;
+        if (it >= DS && !mbar_wait_warp(bar_doempty + ds, ((it / DS) - 1) & 1, wd)) break;
+        if (lane == 0) {
+          mbar_expect_tx(bar_dofull + ds, L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
+                        i * kBlock, bh);
+        }
+        __syncwarp();
+        do_issued = it + 1;
       }
       if (lane == 0) {
         mbar_wait_drain(bar_kv, 0, wait_limit);
-        for (int t = max(0, issued - S); t < issued; ++t)
-          mbar_wait_drain(bar_qfull + (t % S), (t / S) & 1, wait_limit);
+        for (int t = max(0, q_issued - QS); t < q_issued; ++t)
+          mbar_wait_drain(bar_qfull + (t % QS), (t / QS) & 1, wait_limit);
+        for (int t = max(0, do_issued - DS); t < do_issued; ++t)
+          mbar_wait_drain(bar_dofull + (t % DS), (t / DS) & 1, wait_limit);
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-    constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV, dK: A K-major, B MN-major
+    constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
     constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ: A, B MN-major
     const uint32_t k_base = smem_u32(smem + L::kK);
     const uint32_t v_base = smem_u32(smem + L::kV);
     const uint32_t q_base0 = smem_u32(smem + L::kQ);
     const uint32_t do_base0 = smem_u32(smem + L::kDO);
-    const uint32_t p_base = smem_u32(smem + L::kP);
-    const uint32_t ds_base = smem_u32(smem + L::kDS);
+    const uint32_t ds_base = smem_u32(smem + L::kDSb);
     bool ok = n_iter > 0 && mbar_wait_warp(bar_kv, 0, wd);
-    if (ok) tc_fence_after();
-    for (int it = 0; ok && it < n_iter; ++it) {
-      const int s = it % S;
-      const uint32_t q_base = q_base0 + s * L::kTile;
-      const uint32_t do_base = do_base0 + s * L::kTile;
-      if (!mbar_wait_warp(bar_qfull + s, (it / S) & 1, wd)) { ok = false; break; }
-      if (D == 128 && it >= 1 && !mbar_wait_warp(bar_dqfree, (it - 1) & 1, wd)) { ok = false; break; }
+    auto issue_s = [&](int it) -> bool {
+      if (!mbar_wait_warp(bar_qfull + (it % QS), (it / QS) & 1, wd)) return false;
       tc_fence_after();
       if (lane == 0) {
+        const uint32_t qb = q_base0 + (it % QS) * L::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
           mma_ss(tmem + L::kTS, sdesc_sw128(k_base + off, 16, 1024),
-                 sdesc_sw128(q_base + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
+                 sdesc_sw128(qb + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_sfull);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](int it) -> bool {
+      if (!mbar_wait_warp(bar_dofull + (it % DS), (it / DS) & 1, wd)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t db = do_base0 + (it % DS) * L::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
           mma_ss(tmem + L::kTDP, sdesc_sw128(v_base + off, 16, 1024),
-                 sdesc_sw128(do_base + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
+                 sdesc_sw128(db + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_dpfull);
       }
       __syncwarp();
+      return true;
+    };
+    if (ok) {
+      tc_fence_after();
+      ok = issue_s(0) && issue_dp(0);
+    }
+    for (int it = 0; ok && it < n_iter; ++it) {
+      const uint32_t q_base = q_base0 + (it % QS) * L::kTile;
+      const uint32_t do_base = do_base0 + (it % DS) * L::kTile;
+      // dV += P^T dO: P^T (bf16) sits in the S^T columns [0,32) and [64,96)
       if (!mbar_wait_warp(bar_pready, it & 1, wd)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(p_base + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(do_base + kk * 2048, kChunk, 1024);
-          mma_ss(tmem + L::kTDV, a, b, kIdKM, (it > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t a_col = L::kTS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+          mma_ts(tmem + L::kTDV, tmem + a_col, sdesc_sw128(do_base + kk * 2048, kChunk, 1024),
+                 kIdKM, (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar_pfree);
+        mma_commit(bar_doempty + (it % DS));
       }
       __syncwarp();
+      // S^T of the next Q tile while dS of this one is formed
+      if (it + 1 < n_iter && !issue_s(it + 1)) { ok = false; break; }
       if (!mbar_wait_warp(bar_dsready, it & 1, wd)) { ok = false; break; }
       if (D == 64 && it >= 1 && !mbar_wait_warp(bar_dqfree, (it - 1) & 1, wd)) { ok = false; break; }
       tc_fence_after();
@@ -312,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b = sdesc_sw128(q_base + kk * 2048, kChunk, 1024);
           mma_ss(tmem + L::kTDK, a, b, kIdKM, (it > 0 || kk > 0) ? 1u : 0u);
         }
+        mma_commit(bar_qempty + (it % QS));
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
           const uint64_t a = sdesc_sw128(ds_base + kk * 2048, kChunk, 1024);
@@ -320,20 +390,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar_dqfull);
         mma_commit(bar_dsfree);
-        mma_commit(bar_qempty + s);
       }
       __syncwarp();
+      if (it + 1 < n_iter) {
+        // d = 128: dQ_i occupies the dP^T columns until the drain warps have it
+        if (D == 128 && !mbar_wait_warp(bar_dqfree, it & 1, wd)) { ok = false; break; }
+        if (!issue_dp(it + 1)) { ok = false; break; }
+      }
     }
     if (lane == 0) {
       mma_commit(bar_final);
       mbar_wait_drain(bar_final, 0, wait_limit);
     }
     __syncwarp();
-  } else if (warp >= 6) {
-    // ------------------------------------------------------------ dQ drain (warps 6-9)
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ dQ drain (warps 10-13)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // query row within the tile == TMEM lane
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint8_t* stage = smem + L::kDQ;
+    const uint32_t st_base = smem_u32(stage);
+    const bool issuer = (quarter == 0 && lane == 0);
+    constexpr int kRounds = (D / 32) / L::kDQChunks;
     for (int it = 0; it < n_iter; ++it) {
       const int i = i0 + it;
       if (!mbar_wait_warp(bar_dqfull, it & 1, wd)) break;
@@ -347,46 +425,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
-      float4* dst = reinterpret_cast<float4*>(
-          dq_acc + (static_cast<size_t>(bh) * Npad + static_cast<size_t>(i) * kBlock + r) * D);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int round = 0; round < kRounds; ++round) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 add = make_float4(__uint_as_float(v[c][4 * u + 0]) * scale,
-                                         __uint_as_float(v[c][4 * u + 1]) * scale,
-                                         __uint_as_float(v[c][4 * u + 2]) * scale,
-                                         __uint_as_float(v[c][4 * u + 3]) * scale);
-          atomicAdd(dst + c * 8 + u, add);
+        for (int cc = 0; cc < L::kDQChunks; ++cc) {
+          const int c = round * L::kDQChunks + cc;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t addr = st_base + cc * kChunk + r * 128 + (((u ^ (r & 7))) << 4);
+            st_shared_v4(addr, __float_as_uint(__uint_as_float(v[c][4 * u + 0]) * scale),
+                         __float_as_uint(__uint_as_float(v[c][4 * u + 1]) * scale),
+                         __float_as_uint(__uint_as_float(v[c][4 * u + 2]) * scale),
+                         __float_as_uint(__uint_as_float(v[c][4 * u + 3]) * scale));
+          }
         }
+        fence_proxy_async_smem();
+        named_bar_sync(3, 128);
+        if (issuer) {
+#pragma unroll
+          for (int cc = 0; cc < L::kDQChunks; ++cc)
+            tma_reduce_add_3d(&tm_dqacc, stage + cc * kChunk, (round * L::kDQChunks + cc) * 32,
+                              i * kBlock, bh);
+          bulk_commit();
+          bulk_wait_read0();
+        }
+        named_bar_sync(3, 128);
       }
     }
   } else {
-    // ------------------------------------------------------------ P / dS (warps 0-3)
-    const int t = threadIdx.x;  // key row within the tile == TMEM lane
-    const int key = j * kBlock + t;
+    // ------------------------------------------------------------ P / dS (warps 0-7)
+    const int wg = warp >> 2;             // query columns [64 wg, 64 wg + 64)
+    const int quarter = warp & 3;
+    const int kr = quarter * 32 + lane;   // key row within the tile == TMEM lane
+    const int key = j * kBlock + kr;
     const bool key_live = key < kv_bound;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t p_base = smem_u32(smem + L::kP);
-    const uint32_t ds_base = smem_u32(smem + L::kDS);
+    const int qc0 = wg * 64;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t ds_base = smem_u32(smem + L::kDSb) + wg * kChunk;
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
-      const int s = it % S;
+      const int s = it % QS;
       const int i = i0 + it;
-      const float* st_lse = reinterpret_cast<const float*>(smem + L::kStat + s * 1024);
+      const float* st_lse = reinterpret_cast<const float*>(smem + L::kStat + s * 1024) + qc0;
       const float* st_delta = st_lse + 128;
-      if (!mbar_wait_warp(bar_qfull + s, (it / S) & 1, wd)) { ok = false; break; }
+      if (!mbar_wait_warp(bar_qfull + s, (it / QS) & 1, wd)) { ok = false; break; }
       if (!mbar_wait_warp(bar_sfull, it & 1, wd)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + L::kTS + c * 32, r[c]);
+      uint32_t r[2][32];
+      tmem_ld32(lane_base + L::kTS + qc0, r[0]);
+      tmem_ld32(lane_base + L::kTS + qc0 + 32, r[1]);
       tmem_wait_ld();
+      reg_fence(r[0]);
+      reg_fence(r[1]);
+      float p[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence(r[c]);
-      float p[128];
-#pragma unroll
-      for (int c = 0; c < 128; c += 4) {
+      for (int c = 0; c < 64; c += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(st_lse + c);
         p[c + 0] = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 0) & 31]), scale_log2, -l4.x));
         p[c + 1] = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 1) & 31]), scale_log2, -l4.y));
@@ -395,104 +488,93 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!key_live) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) p[c] = 0.f;
+        for (int c = 0; c < 64; ++c) p[c] = 0.f;
       }
       if (CAUSAL && i == j) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < t) p[c] = 0.f;  // query i*128+c < key j*128+t
+        for (int c = 0; c < 64; ++c)
+          if (qc0 + c < kr) p[c] = 0.f;  // query i*128+qc0+c < key j*128+kr
       }
-      if (it >= 1) {
-        if (!mbar_wait_warp(bar_pfree, (it - 1) & 1, wd)) { ok = false; break; }
-      }
-      // P^T row t -> shared memory, K-major (queries along K), 128-byte swizzle.
+      uint32_t pk[32];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const uint32_t addr = p_base + (u >> 3) * kChunk + t * 128 + ((((u & 7) ^ (t & 7))) << 4);
-        st_shared_v4(addr, pack_bf16(p[8 * u + 0], p[8 * u + 1]), pack_bf16(p[8 * u + 2], p[8 * u + 3]),
-                     pack_bf16(p[8 * u + 4], p[8 * u + 5]), pack_bf16(p[8 * u + 6], p[8 * u + 7]));
-      }
-      fence_proxy_async_smem();
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(p[2 * c], p[2 * c + 1]);
+      // P^T over the first 32 of this warpgroup's 64 S^T columns (already read)
+      tmem_st32(lane_base + L::kTS + qc0, pk);
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pready);
 
       if (!mbar_wait_warp(bar_dpfull, it & 1, wd)) { ok = false; break; }
-      if (it >= 1) {
-        if (!mbar_wait_warp(bar_dsfree, (it - 1) & 1, wd)) { ok = false; break; }
-      }
+      if (it >= 1 && !mbar_wait_warp(bar_dsfree, (it - 1) & 1, wd)) { ok = false; break; }
       tc_fence_after();
+      tmem_ld32(lane_base + L::kTDP + qc0, r[0]);
+      tmem_ld32(lane_base + L::kTDP + qc0 + 32, r[1]);
+      tmem_wait_ld();
+      reg_fence(r[0]);
+      reg_fence(r[1]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t dp[32];
-        tmem_ld32(lane_base + L::kTDP + c * 32, dp);
-        tmem_wait_ld();
-        reg_fence(dp);
+      for (int u = 0; u < 8; ++u) {
+        const int q0 = u * 8;
+        const float4 da = *reinterpret_cast<const float4*>(st_delta + q0);
+        const float4 db = *reinterpret_cast<const float4*>(st_delta + q0 + 4);
+        const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+        float g[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int q0 = c * 32 + u * 8;
-          const float4 da = *reinterpret_cast<const float4*>(st_delta + q0);
-          const float4 db = *reinterpret_cast<const float4*>(st_delta + q0 + 4);
-          const float d0 = p[q0 + 0] * (__uint_as_float(dp[u * 8 + 0]) - da.x);
-          const float d1 = p[q0 + 1] * (__uint_as_float(dp[u * 8 + 1]) - da.y);
-          const float d2 = p[q0 + 2] * (__uint_as_float(dp[u * 8 + 2]) - da.z);
-          const float d3 = p[q0 + 3] * (__uint_as_float(dp[u * 8 + 3]) - da.w);
-          const float d4 = p[q0 + 4] * (__uint_as_float(dp[u * 8 + 4]) - db.x);
-          const float d5 = p[q0 + 5] * (__uint_as_float(dp[u * 8 + 5]) - db.y);
-          const float d6 = p[q0 + 6] * (__uint_as_float(dp[u * 8 + 6]) - db.z);
-          const float d7 = p[q0 + 7] * (__uint_as_float(dp[u * 8 + 7]) - db.w);
-          const int unit = q0 >> 3;  // 0..15
-          const uint32_t addr =
-              ds_base + (unit >> 3) * kChunk + t * 128 + ((((unit & 7) ^ (t & 7))) << 4);
-          st_shared_v4(addr, pack_bf16(d0, d1), pack_bf16(d2, d3), pack_bf16(d4, d5),
-                       pack_bf16(d6, d7));
-        }
+        for (int e = 0; e < 8; ++e)
+          g[e] = p[q0 + e] * (__uint_as_float(r[(q0 + e) >> 5][(q0 + e) & 31]) - dd[e]);
+        const uint32_t addr = ds_base + kr * 128 + (((u ^ (kr & 7))) << 4);
+        st_shared_v4(addr, pack_bf16(g[0], g[1]), pack_bf16(g[2], g[3]), pack_bf16(g[4], g[5]),
+                     pack_bf16(g[6], g[7]));
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dsready);
     }
-    // ------------------------------------------------------------ epilogue: dV, dK
+    // ------------------------------------------------------------ epilogue: dV (wg 0), dK (wg 1)
     bool have = ok && n_iter > 0;
     if (have) have = mbar_wait_warp(bar_final, 0, wd);
     if (have) tc_fence_after();
-    const bool row_ok = key < N;
-    const size_t roff = (static_cast<size_t>(bh) * N + key) * D;
+    const uint32_t col = wg == 0 ? L::kTDV : L::kTDK;
+    const float mul = wg == 0 ? 1.f : scale;
+    uint8_t* stage = smem + L::kQ + wg * L::kTile;  // Q stages are free now
+    const uint32_t st_base = smem_u32(stage);
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t col = which == 0 ? L::kTDV : L::kTDK;
-      const float mul = which == 0 ? 1.f : scale;
-      uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + roff);
+    for (int c0 = 0; c0 < D / 32; ++c0) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(lane_base + col + c0 * 32, v);
+        tmem_wait_ld();
+        reg_fence(v);
+      } else {
 #pragma unroll
-      for (int c0 = 0; c0 < D / 32; ++c0) {
-        uint32_t v[32];
-        if (have) {
-          tmem_ld32(lane_base + col + c0 * 32, v);
-          tmem_wait_ld();
-          reg_fence(v);
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] = 0u;
-        }
-        if (row_ok) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul);
-            w.y = pack_bf16(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul);
-            w.z = pack_bf16(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul);
-            w.w = pack_bf16(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul);
-            dst[c0 * 4 + u] = w;
-          }
-        }
+        for (int x = 0; x < 32; ++x) v[x] = 0u;
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int unit = c0 * 4 + u;
+        const uint32_t addr = st_base + (unit >> 3) * kChunk + kr * 128 + (((unit & 7) ^ (kr & 7)) << 4);
+        st_shared_v4(addr,
+                     pack_bf16(__uint_as_float(v[8 * u + 0]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
+                     pack_bf16(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
+                     pack_bf16(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
+                     pack_bf16(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + wg, 128);
+    if (quarter == 0 && lane == 0) {
+      const CUtensorMap* map = wg == 0 ? &tm_dv : &tm_dk;
+      for (int c = 0; c < L::kChunks; ++c) tma_store_3d(map, stage + c * kChunk, c * 64, j * kBlock, bh);
+      bulk_commit();
+      bulk_wait_read0();
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -537,9 +619,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
     kern<<<dim3(nt, a.H, a.B), kThreads, L::kSmem, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc,
-        static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), a.H, a.N, Npad,
-        a.scale, a.kv_len, a.status, a.wait_limit);
+        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, a.tm_dk, a.tm_dv, a.lse2, a.delta, a.H, a.N,
+        Npad, a.scale, a.kv_len, a.status, a.wait_limit);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

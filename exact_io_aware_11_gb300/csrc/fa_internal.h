@@ -29,7 +29,8 @@ struct FwdLaunch {
 };
 
 struct BwdLaunch {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as above
+  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv;  // as above
+  CUtensorMap tm_dqacc;  // fp32 [B*H, Npad, d] accumulator, box 32 x 128 x 1, 128B swizzle
   const void* o;
   const void* dout;
   const float* lse;
