@@ -311,22 +311,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
     constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
     constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ: A, B MN-major
-    const uint32_t k_base = smem_u32(smem + L::kK);
-    const uint32_t v_base = smem_u32(smem + L::kV);
-    const uint32_t q_base0 = smem_u32(smem + L::kQ);
-    const uint32_t do_base0 = smem_u32(smem + L::kDO);
-    const uint32_t ds_base = smem_u32(smem + L::kDSb);
+    // Descriptors built once; per MMA only a compile-time offset is added.
+    const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
+    const uint64_t k_mn = sdesc_sw128(smem_u32(smem + L::kK), kChunk, 1024);
+    const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
+    const uint64_t q_kmaj0 = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+    const uint64_t q_mn0 = sdesc_sw128(smem_u32(smem + L::kQ), kChunk, 1024);
+    const uint64_t do_kmaj0 = sdesc_sw128(smem_u32(smem + L::kDO), 16, 1024);
+    const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + L::kDO), kChunk, 1024);
+    const uint64_t ds_kmaj = sdesc_sw128(smem_u32(smem + L::kDSb), 16, 1024);
+    const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + L::kDSb), kChunk, 1024);
     bool ok = n_iter > 0 && mbar_wait_warp(bar_kv, 0, wd);
     auto issue_s = [&](int it) -> bool {
       if (!mbar_wait_warp(bar_qfull + (it % QS), (it / QS) & 1, wd)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t qb = q_base0 + (it % QS) * L::kTile;
+        const uint64_t qd = desc_adv(q_kmaj0, (it % QS) * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss(tmem + L::kTS, sdesc_sw128(k_base + off, 16, 1024),
-                 sdesc_sw128(qb + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + L::kTS, desc_adv(k_kmaj, off), desc_adv(qd, off), kIdSS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_sfull);
       }
@@ -337,12 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(bar_dofull + (it % DS), (it / DS) & 1, wd)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t db = do_base0 + (it % DS) * L::kTile;
+        const uint64_t dd = desc_adv(do_kmaj0, (it % DS) * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss(tmem + L::kTDP, sdesc_sw128(v_base + off, 16, 1024),
-                 sdesc_sw128(db + off, 16, 1024), kIdSS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + L::kTDP, desc_adv(v_kmaj, off), desc_adv(dd, off), kIdSS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_dpfull);
       }
@@ -354,8 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = issue_s(0) && issue_dp(0);
     }
     for (int it = 0; ok && it < n_iter; ++it) {
-      const uint32_t q_base = q_base0 + (it % QS) * L::kTile;
-      const uint32_t do_base = do_base0 + (it % DS) * L::kTile;
+      const uint64_t q_mn = desc_adv(q_mn0, (it % QS) * L::kTile);
+      const uint64_t do_mn = desc_adv(do_mn0, (it % DS) * L::kTile);
+      const uint32_t acc0 = it > 0 ? 1u : 0u;
       // dV += P^T dO: P^T (bf16) sits in the S^T columns [0,32) and [64,96)
       if (!mbar_wait_warp(bar_pready, it & 1, wd)) { ok = false; break; }
       tc_fence_after();
@@ -363,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
           const uint32_t a_col = L::kTS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + L::kTDV, tmem + a_col, sdesc_sw128(do_base + kk * 2048, kChunk, 1024),
-                 kIdKM, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + L::kTDV, tmem + a_col, desc_adv(do_mn, kk * 2048), kIdKM,
+                 kk > 0 ? 1u : acc0);
         }
         mma_commit(bar_doempty + (it % DS));
       }
@@ -377,16 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(ds_base + (kk >> 2) * kChunk + (kk & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(q_base + kk * 2048, kChunk, 1024);
-          mma_ss(tmem + L::kTDK, a, b, kIdKM, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ss(tmem + L::kTDK, desc_adv(ds_kmaj, (kk >> 2) * kChunk + (kk & 3) * 32),
+                 desc_adv(q_mn, kk * 2048), kIdKM, kk > 0 ? 1u : acc0);
         }
         mma_commit(bar_qempty + (it % QS));
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
-          const uint64_t a = sdesc_sw128(ds_base + kk * 2048, kChunk, 1024);
-          const uint64_t b = sdesc_sw128(k_base + kk * 2048, kChunk, 1024);
-          mma_ss(tmem + L::kTDQ, a, b, kIdMM, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + L::kTDQ, desc_adv(ds_mn, kk * 2048), desc_adv(k_mn, kk * 2048), kIdMM,
+                 kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_dqfull);
         mma_commit(bar_dsfree);

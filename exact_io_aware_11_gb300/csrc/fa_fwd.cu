@@ -237,22 +237,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
     constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
-    const uint32_t q_base = smem_u32(smem + L::kQ);
-    const uint32_t k_base = smem_u32(smem + L::kK);
-    const uint32_t v_base = smem_u32(smem + L::kV);
+    // Descriptors built once; per MMA only a compile-time offset is added.
+    const uint64_t q_desc = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);     // K-major
+    const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
+    const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
     int n_s[2] = {0, 0}, n_pv[2] = {0, 0};
     bool ok = mbar_wait_warp(bar_q, 0, wd);
     auto issue_s = [&](int t, int u) -> bool {
       if (!mbar_wait_warp(bar_kfull + (u % KS), (u / KS) & 1, wd)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t qb = q_base + t * L::kTile;
-        const uint32_t kb = k_base + (u % KS) * L::kTile;
+        const uint64_t qd = desc_adv(q_desc, t * L::kTile);
+        const uint64_t kd = desc_adv(k_desc, (u % KS) * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                 kIdS, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + t * 128, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_sfull + t);
       }
@@ -265,13 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(bar_vfull + (u % VS), (u / VS) & 1, wd)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t vb = v_base + (u % VS) * L::kTile;
+        const uint64_t vd = desc_adv(v_desc, (u % VS) * L::kTile);
+        const uint32_t acc0 = n_pv[t] > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
           // A = P (bf16 pairs in the first 64 columns of S_t), B = V, MN-major.
-          mma_ts(tmem + L::kTO + t * D, tmem + t * 128 + kk * 8,
-                 sdesc_sw128(vb + kk * 2048, kChunk, 1024), kIdO,
-                 (n_pv[t] > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + L::kTO + t * D, tmem + t * 128 + kk * 8, desc_adv(vd, kk * 2048), kIdO,
+                 kk > 0 ? 1u : acc0);
         }
         mma_commit(bar_odone + t);
       }

@@ -238,6 +238,15 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Advances a shared-memory descriptor by `bytes` (a multiple of 16). The start
+// address field holds (address >> 4) in the low 14 bits, so the add is exact
+// while the address stays inside shared memory; issuing threads build each
+// operand's descriptor once and step it with compile-time offsets, which
+// keeps the per-MMA issue cost to a single add.
+__device__ __forceinline__ uint64_t desc_adv(uint64_t d, uint32_t bytes) {
+  return d + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: bf16 x bf16 -> f32 accumulate, dense.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                    // D format: f32
