@@ -132,29 +132,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int nqt = (N + kBlock - 1) / kBlock;
   const int bh = blockIdx.z * H + blockIdx.y;
-  int qtile[2];
+  // Q tiles of this CTA (B = -1 when there is none) and the K/V tiles each visits.
+  int qtA, qtB;
   if (CAUSAL) {
-    qtile[0] = blockIdx.x;
-    qtile[1] = nqt - 1 - static_cast<int>(blockIdx.x);
-    if (qtile[1] == qtile[0]) qtile[1] = -1;
+    qtA = blockIdx.x;
+    qtB = nqt - 1 - static_cast<int>(blockIdx.x);
+    if (qtB == qtA) qtB = -1;
   } else {
-    qtile[0] = 2 * blockIdx.x;
-    qtile[1] = 2 * blockIdx.x + 1 < nqt ? 2 * blockIdx.x + 1 : -1;
+    qtA = 2 * blockIdx.x;
+    qtB = 2 * blockIdx.x + 1 < nqt ? 2 * blockIdx.x + 1 : -1;
   }
   int kv_bound = N;
   if (kv_len != nullptr) kv_bound = min(N, max(0, kv_len[blockIdx.z]));
   const int kv_tiles = (kv_bound + kBlock - 1) / kBlock;
-  TileSet ts[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qt = qtile[t];
-    ts[t].end = qt < 0 ? 0 : (CAUSAL ? min(kv_tiles, qt + 1) : kv_tiles);
-    ts[t].mrow = (block_mask != nullptr && qt >= 0) ? block_mask + static_cast<size_t>(qt) * nqt
-                                                    : nullptr;
-  }
-  const int uend = max(ts[0].end, ts[1].end);
+  const TileSet tsA{CAUSAL ? min(kv_tiles, qtA + 1) : kv_tiles,
+                    block_mask != nullptr ? block_mask + static_cast<size_t>(qtA) * nqt : nullptr};
+  const TileSet tsB{qtB < 0 ? 0 : (CAUSAL ? min(kv_tiles, qtB + 1) : kv_tiles),
+                    (block_mask != nullptr && qtB >= 0) ? block_mask + static_cast<size_t>(qtB) * nqt
+                                                        : nullptr};
+  const int uend = max(tsA.end, tsB.end);
   auto next_union = [&](int j) {
-    while (j < uend && !ts[0].has(j) && !ts[1].has(j)) ++j;
+    while (j < uend && !tsA.has(j) && !tsB.has(j)) ++j;
     return j;
   };
 
@@ -188,44 +186,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Watchdog wd{wait_limit, status, abort_flag};
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    int k_issued = 0, v_issued = 0;
+    // ------------------------------------------------------------ TMA producer (one lane)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_o);
-      mbar_expect_tx(bar_q, (qtile[1] >= 0 ? 2 : 1) * L::kTile);
-      for (int t = 0; t < 2; ++t)
-        if (qtile[t] >= 0)
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kQ + t * L::kTile + c * kChunk, &tm_q, bar_q, c * 64,
-                        qtile[t] * kBlock, bh);
-    }
-    int u = 0;
-    for (int j = next_union(0); j < uend; j = next_union(j + 1), ++u) {
-      const int ks = u % KS, vs = u % VS;
-      if (u >= KS && !mbar_wait_warp(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) break;
-      if (lane == 0) {
+      mbar_expect_tx(bar_q, (qtB >= 0 ? 2 : 1) * L::kTile);
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_3d(smem + L::kQ + c * kChunk, &tm_q, bar_q, c * 64, qtA * kBlock, bh);
+      if (qtB >= 0)
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(smem + L::kQ + L::kTile + c * kChunk, &tm_q, bar_q, c * 64, qtB * kBlock, bh);
+      int k_issued = 0, v_issued = 0;
+      int u = 0;
+      for (int j = next_union(0); j < uend; j = next_union(j + 1), ++u) {
+        const int ks = u % KS, vs = u % VS;
+        if (u >= KS && !mbar_wait(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) break;
         mbar_expect_tx(bar_kfull + ks, L::kTile);
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
                       j * kBlock, bh);
-      }
-      __syncwarp();
-      k_issued = u + 1;
-      if (u >= VS && !mbar_wait_warp(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) break;
-      if (lane == 0) {
+        k_issued = u + 1;
+        if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) break;
         mbar_expect_tx(bar_vfull + vs, L::kTile);
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_3d(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
                       j * kBlock, bh);
+        v_issued = u + 1;
       }
-      __syncwarp();
-      v_issued = u + 1;
-    }
-    // Let every copy in flight land before the CTA can exit (bounded).
-    if (lane == 0) {
+      // Let every copy in flight land before the CTA can exit (bounded).
       mbar_wait_drain(bar_q, 0, wait_limit);
       for (int t = max(0, k_issued - KS); t < k_issued; ++t)
         mbar_wait_drain(bar_kfull + (t % KS), (t / KS) & 1, wait_limit);
@@ -234,19 +224,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
-    constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
-    // Descriptors built once; per MMA only a compile-time offset is added.
-    const uint64_t q_desc = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);     // K-major
-    const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
-    const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
-    int n_s[2] = {0, 0}, n_pv[2] = {0, 0};
-    bool ok = mbar_wait_warp(bar_q, 0, wd);
-    auto issue_s = [&](int t, int u) -> bool {
-      if (!mbar_wait_warp(bar_kfull + (u % KS), (u / KS) & 1, wd)) return false;
-      tc_fence_after();
-      if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (one lane)
+    // The issuing thread sits on the critical path between the two softmax
+    // warpgroups, so it runs alone, waits without warp-wide votes, and places
+    // a tcgen05 fence only after waiting for P (the one cross-thread TMEM
+    // dependency: P_t written by tcgen05.st, and S_t columns read by
+    // tcgen05.ld before S_t(j+1) overwrites them).
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
+      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
+      // Descriptors built once; per MMA only a compile-time offset is added.
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);     // K-major
+      const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
+      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
+      int n_pvA = 0, n_pvB = 0;  // P V MMAs issued per tile
+      bool ok = mbar_wait(bar_q, 0, wd);
+      auto issue_s = [&](int t, int u) -> bool {
+        if (!mbar_wait(bar_kfull + (u % KS), (u / KS) & 1, wd)) return false;
         const uint64_t qd = desc_adv(q_desc, t * L::kTile);
         const uint64_t kd = desc_adv(k_desc, (u % KS) * L::kTile);
 #pragma unroll
@@ -255,18 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + t * 128, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_sfull + t);
-      }
-      __syncwarp();
-      ++n_s[t];
-      return true;
-    };
-    auto issue_pv = [&](int t, int u) -> bool {
-      if (!mbar_wait_warp(bar_pfull + t, n_pv[t] & 1, wd)) return false;
-      if (!mbar_wait_warp(bar_vfull + (u % VS), (u / VS) & 1, wd)) return false;
-      tc_fence_after();
-      if (lane == 0) {
+        return true;
+      };
+      auto issue_pv = [&](int t, int u) -> bool {
+        const int npv = t ? n_pvB : n_pvA;
+        if (!mbar_wait(bar_pfull + t, npv & 1, wd)) return false;
+        if (!mbar_wait(bar_vfull + (u % VS), (u / VS) & 1, wd)) return false;
+        tc_fence_after();
         const uint64_t vd = desc_adv(v_desc, (u % VS) * L::kTile);
-        const uint32_t acc0 = n_pv[t] > 0 ? 1u : 0u;
+        const uint32_t acc0 = npv > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
           // A = P (bf16 pairs in the first 64 columns of S_t), B = V, MN-major.
@@ -274,38 +265,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                  kk > 0 ? 1u : acc0);
         }
         mma_commit(bar_odone + t);
+        if (t) ++n_pvB; else ++n_pvA;
+        return true;
+      };
+      if (ok) {
+        int u = 0;
+        int j = next_union(0);
+        if (j < uend) {
+          if (tsA.has(j)) ok = issue_s(0, 0);
+          if (ok && tsB.has(j)) ok = issue_s(1, 0);
+          if (ok) mma_commit(bar_kempty + 0);
+        }
+        while (ok && j < uend) {
+          const int jn = next_union(j + 1);
+          const int un = u + 1;
+          // tile A: P_A(j) V_j, then S_A(j+1) over the columns P_A(j) just left
+          if (tsA.has(j)) ok = issue_pv(0, u);
+          if (ok && jn < uend && tsA.has(jn)) ok = issue_s(0, un);
+          if (ok && tsB.has(j)) ok = issue_pv(1, u);
+          if (ok) mma_commit(bar_vempty + (u % VS));
+          if (ok && jn < uend && tsB.has(jn)) ok = issue_s(1, un);
+          if (ok && jn < uend) mma_commit(bar_kempty + (un % KS));
+          j = jn;
+          u = un;
+        }
       }
-      __syncwarp();
-      ++n_pv[t];
-      return true;
-    };
-    if (ok) {
-      tc_fence_after();
-      int u = 0;
-      int j = next_union(0);
-      if (j < uend) {
-        for (int t = 0; t < 2 && ok; ++t)
-          if (ts[t].has(j)) ok = issue_s(t, 0);
-        if (ok && lane == 0) mma_commit(bar_kempty + 0);
-        __syncwarp();
-      }
-      while (ok && j < uend) {
-        const int jn = next_union(j + 1);
-        const int un = u + 1;
-        // tile A: P_A(j) V_j, then S_A(j+1) over the columns P_A(j) just left
-        if (ts[0].has(j)) ok = issue_pv(0, u);
-        if (ok && jn < uend && ts[0].has(jn)) ok = issue_s(0, un);
-        if (ok && ts[1].has(j)) ok = issue_pv(1, u);
-        if (ok && lane == 0) mma_commit(bar_vempty + (u % VS));
-        __syncwarp();
-        if (ok && jn < uend && ts[1].has(jn)) ok = issue_s(1, un);
-        if (ok && jn < uend && lane == 0) mma_commit(bar_kempty + (un % KS));
-        __syncwarp();
-        j = jn;
-        u = un;
-      }
-    }
-    if (lane == 0) {
       mma_commit(bar_final);
       mbar_wait_drain(bar_final, 0, wait_limit);
     }
@@ -314,13 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax (warps 0-7)
     const int t = warp >> 2;              // which Q tile
     const int r = threadIdx.x & 127;      // row within the tile == TMEM lane
-    const int qt = qtile[t];
+    const int qt = t ? qtB : qtA;
     if (qt >= 0) {
       const int row = qt * kBlock + r;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
       const uint32_t s_col = t * 128;
       const uint32_t o_col = L::kTO + t * D;
-      const TileSet my = ts[t];
+      const TileSet my = t ? tsB : tsA;
       float m = -INFINITY;  // reference max, log2 units (scale folded in)
       float l = 0.f;        // sum of exp2(s * scale_log2 - m) over visited keys
       bool ok = true;

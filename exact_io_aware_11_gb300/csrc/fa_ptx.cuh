@@ -87,9 +87,9 @@ struct Watchdog {
   volatile int* abort;
 };
 
-static __device__ __noinline__ void watchdog_fire(const Watchdog& wd) {
-  *wd.abort = 1;
-  atomicCAS(wd.status, FA_OK, FA_ERR_DEVICE_TIMEOUT);
+static __device__ __noinline__ void watchdog_fire(int* status, volatile int* abort) {
+  *abort = 1;
+  atomicCAS(status, FA_OK, FA_ERR_DEVICE_TIMEOUT);
 }
 
 // Waits for the phase with the given parity to complete. Returns false if the
@@ -101,7 +101,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (mbar_try_wait(bar, parity)) return true;
     if (*wd.abort) return false;
     if (clock64() - t0 > wd.limit) {
-      watchdog_fire(wd);
+      watchdog_fire(wd.status, wd.abort);
       return false;
     }
   }
@@ -199,6 +199,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
       : "memory");
 }
 
