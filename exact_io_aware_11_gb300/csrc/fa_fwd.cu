@@ -238,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
       const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
       int n_pvA = 0, n_pvB = 0;  // P V MMAs issued per tile
-      bool ok = mbar_wait(bar_q, 0, wd);
+      bool ok = mbar_wait_spin(bar_q, 0, wd);
       auto issue_s = [&](int t, int u) -> bool {
-        if (!mbar_wait(bar_kfull + (u % KS), (u / KS) & 1, wd)) return false;
+        if (!mbar_wait_spin(bar_kfull + (u % KS), (u / KS) & 1, wd)) return false;
         const uint64_t qd = desc_adv(q_desc, t * L::kTile);
         const uint64_t kd = desc_adv(k_desc, (u % KS) * L::kTile);
 #pragma unroll
@@ -253,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int t, int u) -> bool {
         const int npv = t ? n_pvB : n_pvA;
-        if (!mbar_wait(bar_pfull + t, npv & 1, wd)) return false;
-        if (!mbar_wait(bar_vfull + (u % VS), (u / VS) & 1, wd)) return false;
+        if (!mbar_wait_spin(bar_pfull + t, npv & 1, wd)) return false;
+        if (!mbar_wait_spin(bar_vfull + (u % VS), (u / VS) & 1, wd)) return false;
         tc_fence_after();
         const uint64_t vd = desc_adv(v_desc, (u % VS) * L::kTile);
         const uint32_t acc0 = npv > 0 ? 1u : 0u;

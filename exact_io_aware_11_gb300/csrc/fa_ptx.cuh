@@ -117,6 +117,34 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait that polls with the non-blocking test_wait instead of letting
+// the hardware suspend the thread: for a single thread on the critical path
+// (the MMA issuer), which must react to a phase change at once.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*wd.abort) return false;
+    if (clock64() - t0 > wd.limit) {
+      watchdog_fire(wd.status, wd.abort);
+      return false;
+    }
+  }
+}
+
 // Warp-uniform wait: every lane waits, lane 0's verdict is broadcast.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
   bool ok = mbar_wait(bar, parity, wd);
