@@ -258,74 +258,66 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Watchdog wd{wait_limit, status, abort_flag};
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
-    int q_issued = 0, do_issued = 0;
-    if (n_iter > 0) {
-      if (lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_do);
-        tma_prefetch_desc(&tm_dqacc);
-        mbar_expect_tx(bar_kv, 2 * L::kTile);
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_3d(smem + L::kK + c * kChunk, &tm_k, bar_kv, c * 64, j * kBlock, bh);
-          tma_load_3d(smem + L::kV + c * kChunk, &tm_v, bar_kv, c * 64, j * kBlock, bh);
-        }
+    // ------------------------------------------------------------ TMA producer (one lane)
+    if (lane == 0 && n_iter > 0) {
+      int q_issued = 0, do_issued = 0;
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_dqacc);
+      mbar_expect_tx(bar_kv, 2 * L::kTile);
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(smem + L::kK + c * kChunk, &tm_k, bar_kv, c * 64, j * kBlock, bh);
+        tma_load_3d(smem + L::kV + c * kChunk, &tm_v, bar_kv, c * 64, j * kBlock, bh);
       }
       for (int it = 0; it < n_iter; ++it) {
         const int i = i0 + it, qs = it % QS, ds = it % DS;
-        if (it >= QS && !mbar_wait_warp(bar_qempty + qs, ((it / QS) - 1) & 1, wd)) break;
-        if (lane == 0) {
-          mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
-                        i * kBlock, bh);
-          const size_t roff = static_cast<size_t>(bh) * Npad + static_cast<size_t>(i) * kBlock;
-          bulk_load(smem + L::kStat + qs * 1024, lse2 + roff, 512, bar_qfull + qs);
-          bulk_load(smem + L::kStat + qs * 1024 + 512, delta + roff, 512, bar_qfull + qs);
-        }
-        __syncwarp();
+        if (it >= QS && !mbar_wait(bar_qempty + qs, ((it / QS) - 1) & 1, wd)) break;
+        mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
+                      i * kBlock, bh);
+        const size_t roff = static_cast<size_t>(bh) * Npad + static_cast<size_t>(i) * kBlock;
+        bulk_load(smem + L::kStat + qs * 1024, lse2 + roff, 512, bar_qfull + qs);
+        bulk_load(smem + L::kStat + qs * 1024 + 512, delta + roff, 512, bar_qfull + qs);
         q_issued = it + 1;
-        if (it >= DS && !mbar_wait_warp(bar_doempty + ds, ((it / DS) - 1) & 1, wd)) break;
-        if (lane == 0) {
-          mbar_expect_tx(bar_dofull + ds, L::kTile);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
-                        i * kBlock, bh);
-        }
-        __syncwarp();
+        if (it >= DS && !mbar_wait(bar_doempty + ds, ((it / DS) - 1) & 1, wd)) break;
+        mbar_expect_tx(bar_dofull + ds, L::kTile);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
+                      i * kBlock, bh);
         do_issued = it + 1;
       }
-      if (lane == 0) {
-        mbar_wait_drain(bar_kv, 0, wait_limit);
-        for (int t = max(0, q_issued - QS); t < q_issued; ++t)
-          mbar_wait_drain(bar_qfull + (t % QS), (t / QS) & 1, wait_limit);
-        for (int t = max(0, do_issued - DS); t < do_issued; ++t)
-          mbar_wait_drain(bar_dofull + (t % DS), (t / DS) & 1, wait_limit);
-      }
+      mbar_wait_drain(bar_kv, 0, wait_limit);
+      for (int t = max(0, q_issued - QS); t < q_issued; ++t)
+        mbar_wait_drain(bar_qfull + (t % QS), (t / QS) & 1, wait_limit);
+      for (int t = max(0, do_issued - DS); t < do_issued; ++t)
+        mbar_wait_drain(bar_dofull + (t % DS), (t / DS) & 1, wait_limit);
     }
     __syncwarp();
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-    constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
-    constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ: A, B MN-major
-    // Descriptors built once; per MMA only a compile-time offset is added.
-    const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
-    const uint64_t k_mn = sdesc_sw128(smem_u32(smem + L::kK), kChunk, 1024);
-    const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
-    const uint64_t q_kmaj0 = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
-    const uint64_t q_mn0 = sdesc_sw128(smem_u32(smem + L::kQ), kChunk, 1024);
-    const uint64_t do_kmaj0 = sdesc_sw128(smem_u32(smem + L::kDO), 16, 1024);
-    const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + L::kDO), kChunk, 1024);
-    const uint64_t ds_kmaj = sdesc_sw128(smem_u32(smem + L::kDSb), 16, 1024);
-    const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + L::kDSb), kChunk, 1024);
-    bool ok = n_iter > 0 && mbar_wait_warp(bar_kv, 0, wd);
-    auto issue_s = [&](int it) -> bool {
-      if (!mbar_wait_warp(bar_qfull + (it % QS), (it / QS) & 1, wd)) return false;
-      tc_fence_after();
-      if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (one lane)
+    // One thread on the critical path: it polls the barriers (test_wait) and
+    // fences only after the waits that follow tcgen05.ld / tcgen05.st of
+    // other threads (P^T ready, dS ready, dQ drained).
+    if (lane == 0) {
+      constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
+      constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ: A, B MN-major
+      // Descriptors built once; per MMA only a compile-time offset is added.
+      const uint64_t k_kmaj = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
+      const uint64_t k_mn = sdesc_sw128(smem_u32(smem + L::kK), kChunk, 1024);
+      const uint64_t v_kmaj = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
+      const uint64_t q_kmaj0 = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+      const uint64_t q_mn0 = sdesc_sw128(smem_u32(smem + L::kQ), kChunk, 1024);
+      const uint64_t do_kmaj0 = sdesc_sw128(smem_u32(smem + L::kDO), 16, 1024);
+      const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + L::kDO), kChunk, 1024);
+      const uint64_t ds_kmaj = sdesc_sw128(smem_u32(smem + L::kDSb), 16, 1024);
+      const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + L::kDSb), kChunk, 1024);
+      bool ok = n_iter > 0 && mbar_wait_spin(bar_kv, 0, wd);
+      auto issue_s = [&](int it) -> bool {
+        if (!mbar_wait_spin(bar_qfull + (it % QS), (it / QS) & 1, wd)) return false;
         const uint64_t qd = desc_adv(q_kmaj0, (it % QS) * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -333,14 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + L::kTS, desc_adv(k_kmaj, off), desc_adv(qd, off), kIdSS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_sfull);
-      }
-      __syncwarp();
-      return true;
-    };
-    auto issue_dp = [&](int it) -> bool {
-      if (!mbar_wait_warp(bar_dofull + (it % DS), (it / DS) & 1, wd)) return false;
-      tc_fence_after();
-      if (lane == 0) {
+        return true;
+      };
+      auto issue_dp = [&](int it) -> bool {
+        if (!mbar_wait_spin(bar_dofull + (it % DS), (it / DS) & 1, wd)) return false;
         const uint64_t dd = desc_adv(do_kmaj0, (it % DS) * L::kTile);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -348,22 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + L::kTDP, desc_adv(v_kmaj, off), desc_adv(dd, off), kIdSS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar_dpfull);
-      }
-      __syncwarp();
-      return true;
-    };
-    if (ok) {
-      tc_fence_after();
-      ok = issue_s(0) && issue_dp(0);
-    }
-    for (int it = 0; ok && it < n_iter; ++it) {
-      const uint64_t q_mn = desc_adv(q_mn0, (it % QS) * L::kTile);
-      const uint64_t do_mn = desc_adv(do_mn0, (it % DS) * L::kTile);
-      const uint32_t acc0 = it > 0 ? 1u : 0u;
-      // dV += P^T dO: P^T (bf16) sits in the S^T columns [0,32) and [64,96)
-      if (!mbar_wait_warp(bar_pready, it & 1, wd)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
+        return true;
+      };
+      if (ok) ok = issue_s(0) && issue_dp(0);
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const uint64_t q_mn = desc_adv(q_mn0, (it % QS) * L::kTile);
+        const uint64_t do_mn = desc_adv(do_mn0, (it % DS) * L::kTile);
+        const uint32_t acc0 = it > 0 ? 1u : 0u;
+        // dV += P^T dO: P^T (bf16) sits in the S^T columns [0,32) and [64,96)
+        if (!mbar_wait_spin(bar_pready, it & 1, wd)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
           const uint32_t a_col = L::kTS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
@@ -371,14 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                  kk > 0 ? 1u : acc0);
         }
         mma_commit(bar_doempty + (it % DS));
-      }
-      __syncwarp();
-      // S^T of the next Q tile while dS of this one is formed
-      if (it + 1 < n_iter && !issue_s(it + 1)) { ok = false; break; }
-      if (!mbar_wait_warp(bar_dsready, it & 1, wd)) { ok = false; break; }
-      if (D == 64 && it >= 1 && !mbar_wait_warp(bar_dqfree, (it - 1) & 1, wd)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
+        // S^T of the next Q tile while dS of this one is formed
+        if (it + 1 < n_iter && !issue_s(it + 1)) { ok = false; break; }
+        if (!mbar_wait_spin(bar_dsready, it & 1, wd)) { ok = false; break; }
+        if (D == 64 && it >= 1 && !mbar_wait_spin(bar_dqfree, (it - 1) & 1, wd)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
           mma_ss(tmem + L::kTDK, desc_adv(ds_kmaj, (kk >> 2) * kChunk + (kk & 3) * 32),
@@ -392,15 +371,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(bar_dqfull);
         mma_commit(bar_dsfree);
+        if (it + 1 < n_iter) {
+          // d = 128: dQ_i occupies the dP^T columns until the drain warps have it
+          if (D == 128) {
+            if (!mbar_wait_spin(bar_dqfree, it & 1, wd)) { ok = false; break; }
+            tc_fence_after();
+          }
+          if (!issue_dp(it + 1)) { ok = false; break; }
+        }
       }
-      __syncwarp();
-      if (it + 1 < n_iter) {
-        // d = 128: dQ_i occupies the dP^T columns until the drain warps have it
-        if (D == 128 && !mbar_wait_warp(bar_dqfree, it & 1, wd)) { ok = false; break; }
-        if (!issue_dp(it + 1)) { ok = false; break; }
-      }
-    }
-    if (lane == 0) {
       mma_commit(bar_final);
       mbar_wait_drain(bar_final, 0, wait_limit);
     }
