@@ -50,6 +50,30 @@ def peaks():
         return dict(FALLBACK), "fallback"
 
 
+# DRAM bytes (read + write) per launch from one ncu capture, keyed by kernel and
+# workload, valid only while the kernel's source is unchanged (first 16 hex
+# digits of its SHA-256 when it was captured; see profiles/).
+NCU_TRAFFIC = {
+    ("bwd_main", "gpt2_small"): (85_147_904, "fa_bwd.cu", "2ecfa0c73e81fa95"),
+    ("fwd", "gpt2_small"): (37_917_952, "fa_fwd.cu", "cc305a1f9505d983"),
+}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    import hashlib
+    entry = NCU_TRAFFIC.get((kernel, workload))
+    if entry is None:
+        return None
+    nbytes, src, digest = entry
+    path = os.path.join(ROOT, "exact_io_aware_11_gb300", "csrc", src)
+    try:
+        with open(path, "rb") as f:
+            now = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return nbytes if now == digest else None
+
+
 def flops(w: W.Workload, kv_len=None):
     f = 4.0 * w.B * w.H * w.N * w.N * w.d
     if w.causal:
@@ -327,7 +351,8 @@ def run_ours(args, world, rank, local):
         ach = dom_flops / (per_kernel[dom] * 1e-3) / 1e12
         roofline = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2),
                     "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4),
-                    "peak_kind": f"{pk_kind} bf16 dense (burst)", "traffic": None}
+                    "peak_kind": f"{pk_kind} bf16 dense (burst)",
+                    "traffic": ncu_traffic(dom, w.name)}
 
     e2e_ms, h2d, d2h = e2e(fa, step, max(3, args.steps // 4), 3) if w.backward else (None, 0, 0)
     clk = clocks.stop()
