@@ -30,8 +30,9 @@
 // rescaled in TMEM only on those rare tiles; the final O / l is exact because
 // O and l always share the same m.
 //
-// Causal: CTA x pairs Q tiles x and nqt-1-x, so every CTA does the same
-// number of K/V tiles. Otherwise tiles 2x and 2x+1 are paired.
+// CTA x holds Q tiles 2x and 2x+1, so both tiles are active on (almost)
+// every K/V step and their softmax phases alternate on the tensor core;
+// causal grids run the heaviest pairs first.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -133,15 +134,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nqt = (N + kBlock - 1) / kBlock;
   const int bh = blockIdx.z * H + blockIdx.y;
   // Q tiles of this CTA (B = -1 when there is none) and the K/V tiles each visits.
-  int qtA, qtB;
-  if (CAUSAL) {
-    qtA = blockIdx.x;
-    qtB = nqt - 1 - static_cast<int>(blockIdx.x);
-    if (qtB == qtA) qtB = -1;
-  } else {
-    qtA = 2 * blockIdx.x;
-    qtB = 2 * blockIdx.x + 1 < nqt ? 2 * blockIdx.x + 1 : -1;
-  }
+  // Adjacent tiles share a CTA, so both are active on (almost) every K/V step
+  // and their softmax phases can alternate. Causal CTAs run heaviest first.
+  const int pair = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int qtA = 2 * pair;
+  const int qtB = 2 * pair + 1 < nqt ? 2 * pair + 1 : -1;
   int kv_bound = N;
   if (kv_len != nullptr) kv_bound = min(N, max(0, kv_len[blockIdx.z]));
   const int kv_tiles = (kv_bound + kBlock - 1) / kBlock;
