@@ -458,27 +458,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence(r[0]);
       reg_fence(r[1]);
-      float p[64];
+      // P is kept only as bf16 pairs (the form the dV MMA consumes); dS below
+      // unpacks it, which halves the registers a compute thread holds.
+      const bool diag = CAUSAL && i == j;
+      uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(st_lse + c);
-        p[c + 0] = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 0) & 31]), scale_log2, -l4.x));
-        p[c + 1] = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 1) & 31]), scale_log2, -l4.y));
-        p[c + 2] = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 2) & 31]), scale_log2, -l4.z));
-        p[c + 3] = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 3) & 31]), scale_log2, -l4.w));
+        float p0 = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 0) & 31]), scale_log2, -l4.x));
+        float p1 = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 1) & 31]), scale_log2, -l4.y));
+        float p2 = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 2) & 31]), scale_log2, -l4.z));
+        float p3 = ex2(fmaf(__uint_as_float(r[c >> 5][(c + 3) & 31]), scale_log2, -l4.w));
+        if (diag) {  // query i*128+qc0+c < key j*128+kr
+          if (qc0 + c + 0 < kr) p0 = 0.f;
+          if (qc0 + c + 1 < kr) p1 = 0.f;
+          if (qc0 + c + 2 < kr) p2 = 0.f;
+          if (qc0 + c + 3 < kr) p3 = 0.f;
+        }
+        pk[c / 2] = key_live ? pack_bf16(p0, p1) : 0u;
+        pk[c / 2 + 1] = key_live ? pack_bf16(p2, p3) : 0u;
       }
-      if (!key_live) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = 0.f;
-      }
-      if (CAUSAL && i == j) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (qc0 + c < kr) p[c] = 0.f;  // query i*128+qc0+c < key j*128+kr
-      }
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(p[2 * c], p[2 * c + 1]);
       // P^T over the first 32 of this warpgroup's 64 S^T columns (already read)
       tmem_st32(lane_base + L::kTS + qc0, pk);
       tmem_wait_st();
@@ -502,8 +501,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
         float g[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          g[e] = p[q0 + e] * (__uint_as_float(r[(q0 + e) >> 5][(q0 + e) & 31]) - dd[e]);
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t w = pk[(q0 + e) >> 1];
+          const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+          g[e] = pe * (__uint_as_float(r[(q0 + e) >> 5][(q0 + e) & 31]) - dd[e]);
+        }
         const uint32_t addr = ds_base + kr * 128 + (((u ^ (kr & 7))) << 4);
         st_shared_v4(addr, pack_bf16(g[0], g[1]), pack_bf16(g[2], g[3]), pack_bf16(g[4], g[5]),
                      pack_bf16(g[6], g[7]));
