@@ -12,10 +12,13 @@
 // the running statistics in registers and loads every K/V tile once for two
 // Q tiles.
 //
-// One CTA = Q tiles A and B of one (batch, head); 10 warps:
+// The kernel is persistent: one CTA per SM walks a list of work items (Q
+// tiles A = 2p and B = 2p + 1 of one (batch, head)); barrier phases continue
+// across items, so the next item's Q and K/V loads overlap the current one's
+// last steps and epilogue. 10 warps:
 //   warps 0-3   softmax of tile A: thread t owns query row t (= TMEM lane t)
 //   warps 4-7   softmax of tile B
-//   warp 8      TMA producer: Q_A, Q_B once; K_j, V_j through separate rings
+//   warp 8      TMA producer: Q_A, Q_B per item; K_j, V_j through separate rings
 //   warp 9      MMA issuer, in the order
 //                 S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
 //               so that the tensor core computes one tile's MMAs while the
@@ -23,17 +26,20 @@
 // TMEM columns: S_A [0,128), S_B [128,256) (fp32). After reading S_t the
 // softmax writes P_t in bf16 over the first 64 columns of S_t and the PV MMA
 // takes it from there as its A operand, so P never touches shared memory.
-// O_A [256, 256+d), O_B [256+d, 256+2d): fp32 accumulators.
+// O_A [256, 256+d), O_B [256+d, 256+2d): fp32 accumulators; each item ends
+// with O / l stored straight from TMEM to global memory, one row per thread.
 //
 // Rescaling is lazy: a row's reference maximum m only moves when the new
 // tile's maximum exceeds it by more than 8 (log2 units), so P <= 2^8 and O is
 // rescaled in TMEM only on those rare tiles; the final O / l is exact because
 // O and l always share the same m.
 //
-// CTA x holds Q tiles 2x and 2x+1, so both tiles are active on (almost)
-// every K/V step and their softmax phases alternate on the tensor core;
-// causal grids run the heaviest pairs first.
+// An item pairs adjacent Q tiles, so both are active on (almost) every K/V
+// step and their softmax phases alternate on the tensor core; causal items
+// are handed out heaviest first, in a snake order across the CTAs.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -103,58 +109,99 @@ struct TileSet {
   int end;
   const uint8_t* mrow;
   __device__ bool has(int j) const { return j < end && (mrow == nullptr || mrow[j] != 0); }
+  __device__ int last() const {  // last visited tile, -1 if none
+    int j = end - 1;
+    if (mrow != nullptr)
+      while (j >= 0 && mrow[j] == 0) --j;
+    return j;
+  }
 };
+
+// One work item: Q tiles 2p and 2p+1 (B = -1 if absent) of one (batch, head).
+struct FwdItem {
+  int bh, qtA, qtB, kv_bound, uend;
+  TileSet tsA, tsB;
+};
+
+struct FwdGrid {
+  int H, N, nqt, npairs, n_items;
+  const int32_t* kv_len;
+  const uint8_t* block_mask;
+};
+
+// Item k. Causal items are ordered heaviest first (pairs near the diagonal end
+// see the most K/V tiles); otherwise a head's pairs are consecutive.
+template <bool CAUSAL>
+__device__ FwdItem make_item(const FwdGrid& g, int k) {
+  FwdItem it;
+  const int BH = g.n_items / g.npairs;
+  int p;
+  if (CAUSAL) {
+    p = g.npairs - 1 - k / BH;
+    it.bh = k % BH;
+  } else {
+    it.bh = k / g.npairs;
+    p = k % g.npairs;
+  }
+  it.qtA = 2 * p;
+  it.qtB = 2 * p + 1 < g.nqt ? 2 * p + 1 : -1;
+  it.kv_bound = g.N;
+  if (g.kv_len != nullptr) it.kv_bound = min(g.N, max(0, g.kv_len[it.bh / g.H]));
+  const int kv_tiles = (it.kv_bound + kBlock - 1) / kBlock;
+  it.tsA.end = CAUSAL ? min(kv_tiles, it.qtA + 1) : kv_tiles;
+  it.tsA.mrow = g.block_mask != nullptr ? g.block_mask + static_cast<size_t>(it.qtA) * g.nqt : nullptr;
+  it.tsB.end = it.qtB < 0 ? 0 : (CAUSAL ? min(kv_tiles, it.qtB + 1) : kv_tiles);
+  it.tsB.mrow = (g.block_mask != nullptr && it.qtB >= 0)
+                    ? g.block_mask + static_cast<size_t>(it.qtB) * g.nqt
+                    : nullptr;
+  it.uend = max(it.tsA.end, it.tsB.end);
+  return it;
+}
+
+// The r-th item of this CTA: a snake over the (heaviest-first) item list, so
+// that every CTA gets a similar amount of work; -1 when there is none.
+__device__ __forceinline__ int item_of(const FwdGrid& g, int r) {
+  const int G = gridDim.x, c = blockIdx.x;
+  if (r * G >= g.n_items) return -1;
+  const int k = r * G + ((r & 1) ? G - 1 - c : c);
+  return k < g.n_items ? k : -1;  // only the last round can run past the end
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-               float* __restrict__ lse_out, int H, int N, float scale_log2,
-               const int32_t* __restrict__ kv_len, const uint8_t* __restrict__ block_mask,
-               int* status, long long wait_limit) {
+               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+               float* __restrict__ lse_out, FwdGrid g, float scale_log2, int* status,
+               long long wait_limit) {
   using L = FwdLayout<D>;
   constexpr int KS = L::kKS, VS = L::kVS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* bar_q = bars + 0;
-  uint64_t* bar_kfull = bars + 1;    // [KS]
-  uint64_t* bar_kempty = bars + 4;   // [KS]
-  uint64_t* bar_vfull = bars + 7;    // [VS]
-  uint64_t* bar_vempty = bars + 10;  // [VS]
-  uint64_t* bar_sfull = bars + 13;   // [2]
-  uint64_t* bar_pfull = bars + 15;   // [2]
-  uint64_t* bar_odone = bars + 17;   // [2]
-  uint64_t* bar_final = bars + 19;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
-  int* abort_flag = reinterpret_cast<int*>(bars + 21);
+  uint64_t* bar_qfull = bars + 0;    // [2] per Q slot (A, B)
+  uint64_t* bar_qempty = bars + 2;   // [2]
+  uint64_t* bar_kfull = bars + 4;    // [KS]
+  uint64_t* bar_kempty = bars + 7;   // [KS]
+  uint64_t* bar_vfull = bars + 10;   // [VS]
+  uint64_t* bar_vempty = bars + 13;  // [VS]
+  uint64_t* bar_sfull = bars + 16;   // [2]
+  uint64_t* bar_pfull = bars + 18;   // [2]
+  uint64_t* bar_odone = bars + 20;   // [2]
+  uint64_t* bar_final = bars + 22;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
+  int* abort_flag = reinterpret_cast<int*>(bars + 24);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nqt = (N + kBlock - 1) / kBlock;
-  const int bh = blockIdx.z * H + blockIdx.y;
-  // Q tiles of this CTA (B = -1 when there is none) and the K/V tiles each visits.
-  // Adjacent tiles share a CTA, so both are active on (almost) every K/V step
-  // and their softmax phases can alternate. Causal CTAs run heaviest first.
-  const int pair = CAUSAL ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int qtA = 2 * pair;
-  const int qtB = 2 * pair + 1 < nqt ? 2 * pair + 1 : -1;
-  int kv_bound = N;
-  if (kv_len != nullptr) kv_bound = min(N, max(0, kv_len[blockIdx.z]));
-  const int kv_tiles = (kv_bound + kBlock - 1) / kBlock;
-  const TileSet tsA{CAUSAL ? min(kv_tiles, qtA + 1) : kv_tiles,
-                    block_mask != nullptr ? block_mask + static_cast<size_t>(qtA) * nqt : nullptr};
-  const TileSet tsB{qtB < 0 ? 0 : (CAUSAL ? min(kv_tiles, qtB + 1) : kv_tiles),
-                    (block_mask != nullptr && qtB >= 0) ? block_mask + static_cast<size_t>(qtB) * nqt
-                                                        : nullptr};
-  const int uend = max(tsA.end, tsB.end);
-  auto next_union = [&](int j) {
-    while (j < uend && !tsA.has(j) && !tsB.has(j)) ++j;
-    return j;
-  };
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_qfull + t, 1);
+      mbar_init(bar_qempty + t, 1);
+      mbar_init(bar_sfull + t, 1);
+      mbar_init(bar_pfull + t, 4);
+      mbar_init(bar_odone + t, 1);
+    }
     for (int s = 0; s < KS; ++s) {
       mbar_init(bar_kfull + s, 1);
       mbar_init(bar_kempty + s, 1);
@@ -162,11 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < VS; ++s) {
       mbar_init(bar_vfull + s, 1);
       mbar_init(bar_vempty + s, 1);
-    }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar_sfull + t, 1);
-      mbar_init(bar_pfull + t, 4);
-      mbar_init(bar_odone + t, 1);
     }
     mbar_init(bar_final, 1);
     *abort_flag = 0;
@@ -188,32 +230,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_o);
-      mbar_expect_tx(bar_q, (qtB >= 0 ? 2 : 1) * L::kTile);
-      for (int c = 0; c < L::kChunks; ++c)
-        tma_load_3d(smem + L::kQ + c * kChunk, &tm_q, bar_q, c * 64, qtA * kBlock, bh);
-      if (qtB >= 0)
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(smem + L::kQ + L::kTile + c * kChunk, &tm_q, bar_q, c * 64, qtB * kBlock, bh);
+      int nqA = 0, nqB = 0;  // Q loads issued per slot
       int k_issued = 0, v_issued = 0;
-      int u = 0;
-      for (int j = next_union(0); j < uend; j = next_union(j + 1), ++u) {
-        const int ks = u % KS, vs = u % VS;
-        if (u >= KS && !mbar_wait(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) break;
-        mbar_expect_tx(bar_kfull + ks, L::kTile);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
-                      j * kBlock, bh);
-        k_issued = u + 1;
-        if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) break;
-        mbar_expect_tx(bar_vfull + vs, L::kTile);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
-                      j * kBlock, bh);
-        v_issued = u + 1;
+      int u = 0;           // position in the K/V rings, continued across items
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int k = item_of(g, r);
+        if (k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, k);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if ((t ? it.tsB : it.tsA).last() < 0) continue;
+          int& nq = t ? nqB : nqA;
+          if (nq >= 1 && !mbar_wait(bar_qempty + t, (nq - 1) & 1, wd)) { ok = false; break; }
+          mbar_expect_tx(bar_qfull + t, L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kQ + t * L::kTile + c * kChunk, &tm_q, bar_qfull + t, c * 64,
+                        (t ? it.qtB : it.qtA) * kBlock, it.bh);
+          ++nq;
+        }
+        for (int j = 0; ok && j < it.uend; ++j) {
+          if (!it.tsA.has(j) && !it.tsB.has(j)) continue;
+          const int ks = u % KS, vs = u % VS;
+          if (u >= KS && !mbar_wait(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) { ok = false; break; }
+          mbar_expect_tx(bar_kfull + ks, L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
+                        j * kBlock, it.bh);
+          k_issued = u + 1;
+          if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) { ok = false; break; }
+          mbar_expect_tx(bar_vfull + vs, L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
+                        j * kBlock, it.bh);
+          v_issued = u + 1;
+          ++u;
+        }
       }
       // Let every copy in flight land before the CTA can exit (bounded).
-      mbar_wait_drain(bar_q, 0, wait_limit);
+      if (nqA >= 1) mbar_wait_drain(bar_qfull + 0, (nqA - 1) & 1, wait_limit);
+      if (nqB >= 1) mbar_wait_drain(bar_qfull + 1, (nqB - 1) & 1, wait_limit);
       for (int t = max(0, k_issued - KS); t < k_issued; ++t)
         mbar_wait_drain(bar_kfull + (t % KS), (t / KS) & 1, wait_limit);
       for (int t = max(0, v_issued - VS); t < v_issued; ++t)
@@ -223,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer (one lane)
     // The issuing thread sits on the critical path between the two softmax
-    // warpgroups, so it runs alone, waits without warp-wide votes, and places
+    // warpgroups, so it runs alone, polls the barriers (test_wait), and places
     // a tcgen05 fence only after waiting for P (the one cross-thread TMEM
     // dependency: P_t written by tcgen05.st, and S_t columns read by
     // tcgen05.ld before S_t(j+1) overwrites them).
@@ -234,55 +290,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);     // K-major
       const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
       const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
-      int n_pvA = 0, n_pvB = 0;  // P V MMAs issued per tile
-      bool ok = mbar_wait_spin(bar_q, 0, wd);
-      auto issue_s = [&](int t, int u) -> bool {
-        if (!mbar_wait_spin(bar_kfull + (u % KS), (u / KS) & 1, wd)) return false;
-        const uint64_t qd = desc_adv(q_desc, t * L::kTile);
-        const uint64_t kd = desc_adv(k_desc, (u % KS) * L::kTile);
+      // Per-slot state is kept in scalars and slots are compile-time constants
+      // (generic lambdas over std::integral_constant), so nothing of this hot
+      // loop lives in local memory.
+      int npvA = 0, npvB = 0;  // P V MMAs issued per slot (pfull / odone phases)
+      int nqA = 0, nqB = 0;    // Q tiles consumed per slot (qfull phases)
+      int u = 0;               // position in the K/V rings
+      bool ok = true;
+      using SlotA = std::integral_constant<int, 0>;
+      using SlotB = std::integral_constant<int, 1>;
+      for (int r = 0; ok; ++r) {
+        const int k = item_of(g, r);
+        if (k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, k);
+        const int lastA = it.tsA.last(), lastB = it.tsB.last();
+        bool needqA = lastA >= 0, needqB = lastB >= 0;
+        int locA = 0, locB = 0;  // P V MMAs of this item per slot
+        auto issue_s = [&](auto slot, int uu, int j) -> bool {
+          constexpr int t = decltype(slot)::value;
+          bool& needq = t ? needqB : needqA;
+          int& nq = t ? nqB : nqA;
+          if (needq) {
+            if (!mbar_wait_spin(bar_qfull + t, nq & 1, wd)) return false;
+            needq = false;
+          }
+          if (!mbar_wait_spin(bar_kfull + (uu % KS), (uu / KS) & 1, wd)) return false;
+          const uint64_t qd = desc_adv(q_desc, t * L::kTile);
+          const uint64_t kd = desc_adv(k_desc, (uu % KS) * L::kTile);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss(tmem + t * 128, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar_sfull + t);
-        return true;
-      };
-      auto issue_pv = [&](int t, int u) -> bool {
-        const int npv = t ? n_pvB : n_pvA;
-        if (!mbar_wait_spin(bar_pfull + t, npv & 1, wd)) return false;
-        if (!mbar_wait_spin(bar_vfull + (u % VS), (u / VS) & 1, wd)) return false;
-        tc_fence_after();
-        const uint64_t vd = desc_adv(v_desc, (u % VS) * L::kTile);
-        const uint32_t acc0 = npv > 0 ? 1u : 0u;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            mma_ss(tmem + t * 128, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar_sfull + t);
+          if (j == (t ? lastB : lastA)) {  // Q_t of this item is no longer needed
+            mma_commit(bar_qempty + t);
+            ++nq;
+          }
+          return true;
+        };
+        auto issue_pv = [&](auto slot, int uu) -> bool {
+          constexpr int t = decltype(slot)::value;
+          int& npv = t ? npvB : npvA;
+          int& loc = t ? locB : locA;
+          if (!mbar_wait_spin(bar_pfull + t, npv & 1, wd)) return false;
+          if (!mbar_wait_spin(bar_vfull + (uu % VS), (uu / VS) & 1, wd)) return false;
+          tc_fence_after();
+          const uint64_t vd = desc_adv(v_desc, (uu % VS) * L::kTile);
+          const uint32_t acc0 = loc > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk) {
-          // A = P (bf16 pairs in the first 64 columns of S_t), B = V, MN-major.
-          mma_ts(tmem + L::kTO + t * D, tmem + t * 128 + kk * 8, desc_adv(vd, kk * 2048), kIdO,
-                 kk > 0 ? 1u : acc0);
-        }
-        mma_commit(bar_odone + t);
-        if (t) ++n_pvB; else ++n_pvA;
-        return true;
-      };
-      if (ok) {
-        int u = 0;
-        int j = next_union(0);
-        if (j < uend) {
-          if (tsA.has(j)) ok = issue_s(0, 0);
-          if (ok && tsB.has(j)) ok = issue_s(1, 0);
-          if (ok) mma_commit(bar_kempty + 0);
-        }
-        while (ok && j < uend) {
-          const int jn = next_union(j + 1);
+          for (int kk = 0; kk < kBlock / 16; ++kk) {
+            // A = P (bf16 pairs in the first 64 columns of S_t), B = V, MN-major.
+            mma_ts(tmem + L::kTO + t * D, tmem + t * 128 + kk * 8, desc_adv(vd, kk * 2048), kIdO,
+                   kk > 0 ? 1u : acc0);
+          }
+          mma_commit(bar_odone + t);
+          ++npv;
+          ++loc;
+          return true;
+        };
+        int j = 0;
+        while (j < it.uend && !it.tsA.has(j) && !it.tsB.has(j)) ++j;
+        if (j >= it.uend) continue;
+        if (it.tsA.has(j)) ok = issue_s(SlotA{}, u, j);
+        if (ok && it.tsB.has(j)) ok = issue_s(SlotB{}, u, j);
+        if (ok) mma_commit(bar_kempty + (u % KS));
+        while (ok && j < it.uend) {
+          int jn = j + 1;
+          while (jn < it.uend && !it.tsA.has(jn) && !it.tsB.has(jn)) ++jn;
           const int un = u + 1;
           // tile A: P_A(j) V_j, then S_A(j+1) over the columns P_A(j) just left
-          if (tsA.has(j)) ok = issue_pv(0, u);
-          if (ok && jn < uend && tsA.has(jn)) ok = issue_s(0, un);
-          if (ok && tsB.has(j)) ok = issue_pv(1, u);
+          if (it.tsA.has(j)) ok = issue_pv(SlotA{}, u);
+          if (ok && jn < it.uend && it.tsA.has(jn)) ok = issue_s(SlotA{}, un, jn);
+          if (ok && it.tsB.has(j)) ok = issue_pv(SlotB{}, u);
           if (ok) mma_commit(bar_vempty + (u % VS));
-          if (ok && jn < uend && tsB.has(jn)) ok = issue_s(1, un);
-          if (ok && jn < uend) mma_commit(bar_kempty + (un % KS));
+          if (ok && jn < it.uend && it.tsB.has(jn)) ok = issue_s(SlotB{}, un, jn);
+          if (ok && jn < it.uend) mma_commit(bar_kempty + (un % KS));
           j = jn;
           u = un;
         }
@@ -293,22 +376,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax (warps 0-7)
-    const int t = warp >> 2;              // which Q tile
+    const int t = warp >> 2;              // which Q slot
     const int r = threadIdx.x & 127;      // row within the tile == TMEM lane
-    const int qt = t ? qtB : qtA;
-    if (qt >= 0) {
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_col = t * 128;
+    const uint32_t o_col = L::kTO + t * D;
+    int ns = 0;  // S tiles of this slot consumed so far (sfull / pfull / odone phases)
+    bool ok = true;
+    for (int ri = 0; ok; ++ri) {
+      const int k = item_of(g, ri);
+      if (k < 0) break;
+      const FwdItem it = make_item<CAUSAL>(g, k);
+      const int qt = t ? it.qtB : it.qtA;
+      if (qt < 0) continue;
+      const TileSet my = t ? it.tsB : it.tsA;
+      const int kv_bound = it.kv_bound;
       const int row = qt * kBlock + r;
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-      const uint32_t s_col = t * 128;
-      const uint32_t o_col = L::kTO + t * D;
-      const TileSet my = t ? tsB : tsA;
       float m = -INFINITY;  // reference max, log2 units (scale folded in)
       float l = 0.f;        // sum of exp2(s * scale_log2 - m) over visited keys
-      bool ok = true;
-      int n = 0;
+      int n = 0;            // tiles of this item
       for (int j = 0; j < my.end; ++j) {
         if (!my.has(j)) continue;
-        if (!mbar_wait_warp(bar_sfull + t, n & 1, wd)) {
+        if (!mbar_wait_warp(bar_sfull + t, ns & 1, wd)) {
           ok = false;
           break;
         }
@@ -361,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(lane_base + s_col, *reinterpret_cast<uint32_t(*)[32]>(pk));
         tmem_st32(lane_base + s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         if (n >= 1 && __any_sync(0xffffffffu, grow)) {
-          // O must be quiescent (P_t(n-1) V done) before it is rescaled.
-          if (!mbar_wait_warp(bar_odone + t, (n - 1) & 1, wd)) {
+          // O must be quiescent (this item's previous P V done) before it is rescaled.
+          if (!mbar_wait_warp(bar_odone + t, (ns - 1) & 1, wd)) {
             ok = false;
             break;
           }
@@ -385,17 +474,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_pfull + t);
         ++n;
+        ++ns;
       }
+      if (!ok) break;
       // ---------------------------------------------------------- epilogue
-      bool have = ok && n > 0;
-      if (have) have = mbar_wait_warp(bar_odone + t, (n - 1) & 1, wd);
-      if (have) tc_fence_after();
+      // O / l straight from TMEM to global memory (one row per thread); the
+      // next item's first P V overwrites O only after this thread's next P
+      // arrives, i.e. after these loads.
+      bool have = n > 0;
+      if (have) {
+        if (!mbar_wait_warp(bar_odone + t, (ns - 1) & 1, wd)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
       const bool live = have && l > 0.f;
       const float inv = live ? 1.f / l : 0.f;
-      // O row -> the Q_t buffer (free now), same 128-byte swizzled layout as Q,
-      // then one TMA store per 64-column chunk (rows >= N are clipped).
-      uint8_t* stage = smem + L::kQ + t * L::kTile;
-      const uint32_t st_base = smem_u32(stage);
+      const bool row_ok = row < g.N;
+      uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(it.bh) * g.N + row) * D);
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
         uint32_t o[32];
@@ -407,26 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0u;
         }
+        if (row_ok) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int unit = c0 * 4 + v;  // 16-byte unit of the row (8 columns)
-          const uint32_t addr = st_base + (unit >> 3) * kChunk + r * 128 + (((unit & 7) ^ (r & 7)) << 4);
-          st_shared_v4(addr,
-                       pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
-                       pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
-                       pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
-                       pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+            orow[c0 * 4 + v] = w;
+          }
         }
       }
-      if (row < N)
-        lse_out[static_cast<size_t>(bh) * N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
-      fence_proxy_async_smem();
-      named_bar_sync(1 + t, 128);
-      if (r == 0) {
-        for (int c = 0; c < L::kChunks; ++c) tma_store_3d(&tm_o, stage + c * kChunk, c * 64, qt * kBlock, bh);
-        bulk_commit();
-        bulk_wait_read0();
-      }
+      if (row_ok)
+        lse_out[static_cast<size_t>(it.bh) * g.N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -438,18 +529,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+int sm_count() {
+  static int count[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (count[dev] == 0) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) c = 148;
+    count[dev] = c;
+  }
+  return count[dev];
+}
+
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
   auto kern = fwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  const int nqt = (a.N + kBlock - 1) / kBlock;
-  const dim3 grid((nqt + 1) / 2, a.H, a.B);
+  FwdGrid g;
+  g.H = a.H;
+  g.N = a.N;
+  g.nqt = (a.N + kBlock - 1) / kBlock;
+  g.npairs = (g.nqt + 1) / 2;
+  g.n_items = a.B * a.H * g.npairs;
+  g.kv_len = a.kv_len;
+  g.block_mask = a.block_mask;
+  const int grid = min(g.n_items, sm_count());
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, L::kSmem, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.lse, a.H, a.N,
-                                             scale_log2, a.kv_len, a.block_mask, a.status,
-                                             a.wait_limit);
+  kern<<<grid, kThreads, L::kSmem, stream>>>(a.tm_q, a.tm_k, a.tm_v, static_cast<__nv_bfloat16*>(a.o),
+                                             a.lse, g, scale_log2, a.status, a.wait_limit);
   return cudaGetLastError();
 }
 
