@@ -218,8 +218,6 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
   if (mainst && (!encode_bhnd(&a.tm_q, p.q, B, H, N, d) || !encode_bhnd(&a.tm_k, p.k, B, H, N, d) ||
                  !encode_bhnd(&a.tm_v, p.v, B, H, N, d) ||
                  !encode_bhnd(&a.tm_do, p.dout, B, H, N, d) ||
-                 !encode_bhnd(&a.tm_dk, p.dk, B, H, N, d) ||
-                 !encode_bhnd(&a.tm_dv, p.dv, B, H, N, d) ||
                  !encode_f32_rows(&a.tm_dqacc, wsb + ws.dq_off, B * H, npad, d)))
     return FA_ERR_CUDA;
   a.o = p.o;
@@ -255,6 +253,18 @@ BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
   w.delta_off = w.lse2_off + up(rows * 4);
   w.total = w.delta_off + up(rows * 4);
   return w;
+}
+
+int sm_count() {
+  static int count[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (count[dev] == 0) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) c = 148;
+    count[dev] = c;
+  }
+  return count[dev];
 }
 
 }  // namespace fa

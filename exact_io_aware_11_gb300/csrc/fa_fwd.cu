@@ -529,18 +529,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-int sm_count() {
-  static int count[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (count[dev] == 0) {
-    int c = 0;
-    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c < 1) c = 148;
-    count[dev] = c;
-  }
-  return count[dev];
-}
-
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   using L = FwdLayout<D>;

@@ -29,7 +29,7 @@ struct FwdLaunch {
 };
 
 struct BwdLaunch {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv;  // as above
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as above
   CUtensorMap tm_dqacc;  // fp32 [B*H, Npad, d] accumulator, box 32 x 128 x 1, 128B swizzle
   const void* o;
   const void* dout;
@@ -53,6 +53,9 @@ struct BwdWorkspace {
   size_t dq_off, lse2_off, delta_off, total;
 };
 BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d);
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 // Backward stages (bit set): preprocess, main kernel, dQ conversion.

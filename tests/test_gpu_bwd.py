@@ -94,3 +94,28 @@ def test_bwd_workspace_contents_ignored(fa):
     for a, b in zip(g1[1:], g2[1:]):
         assert torch.equal(a, b)
     assert torch.allclose(g1[0].float(), g2[0].float(), rtol=0, atol=1e-2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_many_items_per_cta(fa, causal, d):
+    # 64 x 5 heads x 3 key tiles = 960 work items, so every CTA handles
+    # several, and consecutive items of one CTA mix key tiles that see every
+    # Q tile, tiles that see one, and tiles with no valid key at all (key
+    # padding down to a single key): their dK/dV must come out as zeros.
+    B, H, N = 64, 5, 300
+    w = W.Workload("generic", B, H, N, d, causal=causal, backward=True, std=0.5)
+    x = W.make_inputs(w, 10)
+    g = np.random.default_rng(10)
+    kv = torch.from_numpy(g.integers(1, N + 1, B).astype(np.int32))
+    kv[3] = N
+    kv[7] = 1
+    kv[11] = 129
+    kv[12] = 128
+    grads = run(fa, x, causal, w.scale, kv)
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, causal=causal,
+                          kv_len=kv.numpy())
+    check_grads(grads, ref, f"many items d={d} causal={causal}")
+    dk, dv = f64(grads[1]), f64(grads[2])
+    for b, L in enumerate(kv.tolist()):
+        assert np.all(dk[b, :, L:] == 0) and np.all(dv[b, :, L:] == 0)
