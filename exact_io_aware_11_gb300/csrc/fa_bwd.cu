@@ -72,17 +72,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return p + ((1024u - (a & 1023u)) & 1023u);
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
                                                   int y, int z) {
   asm volatile(
@@ -392,11 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer (one lane)
-    // One thread on the critical path: it polls the barriers (test_wait) and
-    // fences only after the waits that follow tcgen05.ld / tcgen05.st of
-    // other threads (P^T ready, dS ready, dQ drained, dV/dK read out).
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    // On the critical path: the warp runs converged and an elected lane issues
+    // each tcgen05.mma / commit; it polls the barriers (test_wait) and fences
+    // only after the waits that follow tcgen05.ld / tcgen05.st of other
+    // threads (P^T ready, dS ready, dQ drained, dV/dK read out).
+    {
       constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
       constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
       constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ: A, B MN-major
@@ -413,30 +403,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + L::kDSb), kChunk, 1024);
       using Cur = BwdCursor<CAUSAL>;
       auto kv_ready = [&](const Cur& c) -> bool {
-        return mbar_wait_spin(bar_kvfull + (c.t % KVS), (c.t / KVS) & 1, wd);
+        return mbar_wait_spin_w(bar_kvfull + (c.t % KVS), (c.t / KVS) & 1, wd);
       };
       auto issue_s = [&](const Cur& c) -> bool {
-        if (!mbar_wait_spin(bar_qfull + (c.g % QS), (c.g / QS) & 1, wd)) return false;
+        if (!mbar_wait_spin_w(bar_qfull + (c.g % QS), (c.g / QS) & 1, wd)) return false;
         const uint64_t qd = desc_adv(q_kmaj0, (c.g % QS) * L::kTile);
         const uint64_t kd = desc_adv(k_kmaj0, (c.t % KVS) * kKVStride);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss(tmem + L::kTS, desc_adv(kd, off), desc_adv(qd, off), kIdSS, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + L::kTS, desc_adv(kd, off), desc_adv(qd, off), kIdSS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_sfull);
+        mma_commit_w(bar_sfull);
         return true;
       };
       auto issue_dp = [&](const Cur& c) -> bool {
-        if (!mbar_wait_spin(bar_dofull + (c.g % DS), (c.g / DS) & 1, wd)) return false;
+        if (!mbar_wait_spin_w(bar_dofull + (c.g % DS), (c.g / DS) & 1, wd)) return false;
         const uint64_t dd = desc_adv(do_kmaj0, (c.g % DS) * L::kTile);
         const uint64_t vd = desc_adv(v_kmaj0, (c.t % KVS) * kKVStride);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss(tmem + L::kTDP, desc_adv(vd, off), desc_adv(dd, off), kIdSS, kk > 0 ? 1u : 0u);
+          mma_ss_w(tmem + L::kTDP, desc_adv(vd, off), desc_adv(dd, off), kIdSS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_dpfull);
+        mma_commit_w(bar_dpfull);
         return true;
       };
       Cur cur;
@@ -452,53 +442,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t k_mn = desc_adv(k_mn0, (cur.t % KVS) * kKVStride);
         const uint32_t acc0 = first ? 0u : 1u;
         // dV += P^T dO: P^T (bf16) sits in the S^T columns [0,32) and [64,96)
-        if (!mbar_wait_spin(bar_pready, gq & 1, wd)) { ok = false; break; }
-        if (first && cur.t >= 1 && !mbar_wait_spin(bar_dvempty, (cur.t - 1) & 1, wd)) { ok = false; break; }
+        if (!mbar_wait_spin_w(bar_pready, gq & 1, wd)) { ok = false; break; }
+        if (first && cur.t >= 1 && !mbar_wait_spin_w(bar_dvempty, (cur.t - 1) & 1, wd)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
           const uint32_t a_col = L::kTS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts(tmem + L::kTDV, tmem + a_col, desc_adv(do_mn, kk * 2048), kIdKM,
+          mma_ts_w(tmem + L::kTDV, tmem + a_col, desc_adv(do_mn, kk * 2048), kIdKM,
                  kk > 0 ? 1u : acc0);
         }
-        mma_commit(bar_doempty + (gq % DS));
+        mma_commit_w(bar_doempty + (gq % DS));
         // S^T of the next Q tile while dS of this one is formed. Across items
         // with a single K/V stage it must wait until this item's dQ is issued.
         const bool hoist = nx.valid && (KVS > 1 || !last);
         if (hoist && !((nx.it > 0 || kv_ready(nx)) && issue_s(nx))) { ok = false; break; }
-        if (!mbar_wait_spin(bar_dsready, gq & 1, wd)) { ok = false; break; }
-        if (D == 64 && gq >= 1 && !mbar_wait_spin(bar_dqfree, (gq - 1) & 1, wd)) { ok = false; break; }
-        if (first && cur.t >= 1 && !mbar_wait_spin(bar_dkempty, (cur.t - 1) & 1, wd)) { ok = false; break; }
+        if (!mbar_wait_spin_w(bar_dsready, gq & 1, wd)) { ok = false; break; }
+        if (D == 64 && gq >= 1 && !mbar_wait_spin_w(bar_dqfree, (gq - 1) & 1, wd)) { ok = false; break; }
+        if (first && cur.t >= 1 && !mbar_wait_spin_w(bar_dkempty, (cur.t - 1) & 1, wd)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
-          mma_ss(tmem + L::kTDK, desc_adv(ds_kmaj, (kk >> 2) * kChunk + (kk & 3) * 32),
+          mma_ss_w(tmem + L::kTDK, desc_adv(ds_kmaj, (kk >> 2) * kChunk + (kk & 3) * 32),
                  desc_adv(q_mn, kk * 2048), kIdKM, kk > 0 ? 1u : acc0);
         }
-        mma_commit(bar_qempty + (gq % QS));
+        mma_commit_w(bar_qempty + (gq % QS));
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk) {
-          mma_ss(tmem + L::kTDQ, desc_adv(ds_mn, kk * 2048), desc_adv(k_mn, kk * 2048), kIdMM,
+          mma_ss_w(tmem + L::kTDQ, desc_adv(ds_mn, kk * 2048), desc_adv(k_mn, kk * 2048), kIdMM,
                  kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar_dqfull);
-        mma_commit(bar_dsfree);
+        mma_commit_w(bar_dqfull);
+        mma_commit_w(bar_dsfree);
         if (last) {
-          mma_commit(bar_accfull);
-          mma_commit(bar_kvempty + (cur.t % KVS));
+          mma_commit_w(bar_accfull);
+          mma_commit_w(bar_kvempty + (cur.t % KVS));
         }
         if (nx.valid) {
           if (!hoist && !(kv_ready(nx) && issue_s(nx))) { ok = false; break; }
           // d = 128: dQ occupies the dP^T columns until the drain warps have it
           if (D == 128) {
-            if (!mbar_wait_spin(bar_dqfree, gq & 1, wd)) { ok = false; break; }
+            if (!mbar_wait_spin_w(bar_dqfree, gq & 1, wd)) { ok = false; break; }
             tc_fence_after();
           }
           if (!issue_dp(nx)) { ok = false; break; }
         }
         cur = nx;
       }
-      mma_commit(bar_final);
+      mma_commit_w(bar_final);
       mbar_wait_drain(bar_final, 0, wait_limit);
     }
     __syncwarp();

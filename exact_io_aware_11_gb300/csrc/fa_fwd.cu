@@ -16,18 +16,24 @@
 // tiles A = 2p and B = 2p + 1 of one (batch, head)); barrier phases continue
 // across items, so the next item's Q and K/V loads overlap the current one's
 // last steps and epilogue. 10 warps:
-//   warps 0-3   softmax of tile A: thread t owns query row t (= TMEM lane t)
-//   warps 4-7   softmax of tile B
-//   warp 8      TMA producer: Q_A, Q_B per item; K_j, V_j through separate rings
-//   warp 9      MMA issuer, in the order
+//   warp 0      MMA issuer (below)
+//   warp 1      TMA producer: Q_A, Q_B per item; K_j, V_j through separate rings
+//   warps 2-5   softmax of tile A: each thread owns one query row, the TMEM
+//               lane of its warp's quarter (warp % 4)
+//   warps 6-9   softmax of tile B
+//   The MMA issuer runs, at d = 128, in the order
 //                 S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
 //               so that the tensor core computes one tile's MMAs while the
 //               other tile's softmax runs.
-// TMEM columns: S_A [0,128), S_B [128,256) (fp32). After reading S_t the
-// softmax writes P_t in bf16 over the first 64 columns of S_t and the PV MMA
-// takes it from there as its A operand, so P never touches shared memory.
-// O_A [256, 256+d), O_B [256+d, 256+2d): fp32 accumulators; each item ends
-// with O / l stored straight from TMEM to global memory, one row per thread.
+// TMEM columns: S_A [0,128), S_B [128,256) (fp32); O_A [256, 256+d),
+// O_B [256+d, 256+2d) (fp32 accumulators). The softmax writes P_t in bf16
+// pairs to TMEM and the PV MMA takes it from there as its A operand, so P never
+// touches shared memory. At d = 64, P_A and P_B have columns of their own
+// ([384,448), [448,512)): S_t(j+1) is then issued as soon as the softmax has
+// loaded S_t(j) into registers and is ready when P_t(j) is, and the issue
+// order becomes S_A(j+1) S_B(j+1) PV_A(j) PV_B(j). At d = 128 TMEM is full and
+// P_t goes over the first 64 columns of S_t. Each item ends with O / l stored
+// straight from TMEM to global memory, one row per thread.
 //
 // Rescaling is lazy: a row's reference maximum m only moves when the new
 // tile's maximum exceeds it by more than 8 (log2 units), so P <= 2^8 and O is
@@ -48,23 +54,34 @@ namespace fa {
 namespace {
 
 constexpr int kThreads = 320;
+// Warp roles. The MMA issuer is warp 0: among eligible warps the scheduler
+// favours lower warp ids, and the issuer competes for issue slots with two
+// softmax warps on its sub-partition.
+constexpr int kMmaWarp = 0, kLoadWarp = 1, kSoftWarp0 = 2;
 constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled chunk (64 bf16 cols)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 
 template <int D>
 struct FwdLayout {
+  // d = 64 leaves TMEM room for P in columns of its own: the next S of a tile
+  // can then be computed while the softmax of the current one still runs.
+  static constexpr bool kSepP = (D == 64);
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kChunks * kChunk;  // one 128 x D bf16 tile
   static constexpr int kKS = 3;                   // K ring slots
   static constexpr int kVS = (D == 128) ? 2 : 3;  // V ring slots
-  static constexpr int kQ = 0;                    // Q_A, Q_B (reused to stage O)
-  static constexpr int kK = kQ + 2 * kTile;
+  static constexpr int kQS = (D == 128) ? 1 : 2;  // Q stages per tile slot
+  static constexpr int kQ = 0;                    // Q of slot t, stage s: kQ + (t kQS + s) kTile
+  static constexpr int kK = kQ + 2 * kQS * kTile;
   static constexpr int kV = kK + kKS * kTile;
   static constexpr int kBar = kV + kVS * kTile;
   static constexpr int kEnd = kBar + 256;
   static constexpr int kSmem = kEnd + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t kTO = 256;       // O_A; O_B at kTO + D
+  // P_t (bf16 pairs, 64 columns): its own columns, or over the first 64 of S_t
+  static constexpr uint32_t kTP = kSepP ? 256 + 2 * D : 0;
+  __host__ __device__ static constexpr uint32_t p_col(int t) { return kSepP ? kTP + t * 64 : t * 128; }
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -76,17 +93,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   float m;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
   return m;
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
 }
 
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
@@ -174,33 +180,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                float* __restrict__ lse_out, FwdGrid g, float scale_log2, int* status,
                long long wait_limit) {
   using L = FwdLayout<D>;
-  constexpr int KS = L::kKS, VS = L::kVS;
+  constexpr int KS = L::kKS, VS = L::kVS, QS = L::kQS;
+  constexpr bool kSepP = L::kSepP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* bar_qfull = bars + 0;    // [2] per Q slot (A, B)
-  uint64_t* bar_qempty = bars + 2;   // [2]
-  uint64_t* bar_kfull = bars + 4;    // [KS]
-  uint64_t* bar_kempty = bars + 7;   // [KS]
-  uint64_t* bar_vfull = bars + 10;   // [VS]
-  uint64_t* bar_vempty = bars + 13;  // [VS]
-  uint64_t* bar_sfull = bars + 16;   // [2]
-  uint64_t* bar_pfull = bars + 18;   // [2]
-  uint64_t* bar_odone = bars + 20;   // [2]
-  uint64_t* bar_final = bars + 22;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
-  int* abort_flag = reinterpret_cast<int*>(bars + 24);
+  uint64_t* bar_qfull = bars + 0;    // [2][QS] per Q slot (A, B) and stage
+  uint64_t* bar_qempty = bars + 4;   // [2][QS]
+  uint64_t* bar_kfull = bars + 8;    // [KS]
+  uint64_t* bar_kempty = bars + 11;  // [KS]
+  uint64_t* bar_vfull = bars + 14;   // [VS]
+  uint64_t* bar_vempty = bars + 17;  // [VS]
+  uint64_t* bar_sfull = bars + 20;   // [2]
+  uint64_t* bar_pfull = bars + 22;   // [2]
+  uint64_t* bar_odone = bars + 24;   // [2]
+  uint64_t* bar_sfree = bars + 26;   // [2] S_t read out of TMEM (separate-P layout)
+  uint64_t* bar_final = bars + 28;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
+  int* abort_flag = reinterpret_cast<int*>(bars + 30);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
-      mbar_init(bar_qfull + t, 1);
-      mbar_init(bar_qempty + t, 1);
+      for (int q = 0; q < QS; ++q) {
+        mbar_init(bar_qfull + t * QS + q, 1);
+        mbar_init(bar_qempty + t * QS + q, 1);
+      }
       mbar_init(bar_sfull + t, 1);
       mbar_init(bar_pfull + t, 4);
       mbar_init(bar_odone + t, 1);
+      mbar_init(bar_sfree + t, 4);
     }
     for (int s = 0; s < KS; ++s) {
       mbar_init(bar_kfull + s, 1);
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -224,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Watchdog wd{wait_limit, status, abort_flag};
 
-  if (warp == 8) {
+  if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer (one lane)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -242,10 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           if ((t ? it.tsB : it.tsA).last() < 0) continue;
           int& nq = t ? nqB : nqA;
-          if (nq >= 1 && !mbar_wait(bar_qempty + t, (nq - 1) & 1, wd)) { ok = false; break; }
-          mbar_expect_tx(bar_qfull + t, L::kTile);
+          const int qb = t * QS + nq % QS;
+          if (nq >= QS && !mbar_wait(bar_qempty + qb, ((nq / QS) - 1) & 1, wd)) { ok = false; break; }
+          mbar_expect_tx(bar_qfull + qb, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kQ + t * L::kTile + c * kChunk, &tm_q, bar_qfull + t, c * 64,
+            tma_load_3d(smem + L::kQ + qb * L::kTile + c * kChunk, &tm_q, bar_qfull + qb, c * 64,
                         (t ? it.qtB : it.qtA) * kBlock, it.bh);
           ++nq;
         }
@@ -268,22 +280,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Let every copy in flight land before the CTA can exit (bounded).
-      if (nqA >= 1) mbar_wait_drain(bar_qfull + 0, (nqA - 1) & 1, wait_limit);
-      if (nqB >= 1) mbar_wait_drain(bar_qfull + 1, (nqB - 1) & 1, wait_limit);
+      for (int t = 0; t < 2; ++t) {
+        const int nq = t ? nqB : nqA;
+        for (int q = max(0, nq - QS); q < nq; ++q)
+          mbar_wait_drain(bar_qfull + t * QS + q % QS, (q / QS) & 1, wait_limit);
+      }
       for (int t = max(0, k_issued - KS); t < k_issued; ++t)
         mbar_wait_drain(bar_kfull + (t % KS), (t / KS) & 1, wait_limit);
       for (int t = max(0, v_issued - VS); t < v_issued; ++t)
         mbar_wait_drain(bar_vfull + (t % VS), (t / VS) & 1, wait_limit);
     }
     __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer (one lane)
-    // The issuing thread sits on the critical path between the two softmax
-    // warpgroups, so it runs alone, polls the barriers (test_wait), and places
-    // a tcgen05 fence only after waiting for P (the one cross-thread TMEM
-    // dependency: P_t written by tcgen05.st, and S_t columns read by
-    // tcgen05.ld before S_t(j+1) overwrites them).
-    if (lane == 0) {
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    // The issuer sits on the critical path between the two softmax
+    // warpgroups. The warp runs converged and an elected lane issues each
+    // tcgen05.mma / commit; it polls the barriers (test_wait) and places a
+    // tcgen05 fence only after waiting on another thread's TMEM access (P_t
+    // written by tcgen05.st; S_t read by tcgen05.ld before S_t(j+1) overwrites
+    // it).
+    {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
       // Descriptors built once; per MMA only a compile-time offset is added.
@@ -295,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // loop lives in local memory.
       int npvA = 0, npvB = 0;  // P V MMAs issued per slot (pfull / odone phases)
       int nqA = 0, nqB = 0;    // Q tiles consumed per slot (qfull phases)
+      int nsA = 0, nsB = 0;    // S tiles issued per slot (sfree phases)
       int u = 0;               // position in the K/V rings
       bool ok = true;
       using SlotA = std::integral_constant<int, 0>;
@@ -310,21 +327,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           constexpr int t = decltype(slot)::value;
           bool& needq = t ? needqB : needqA;
           int& nq = t ? nqB : nqA;
+          int& ns = t ? nsB : nsA;
+          const int qb = t * QS + nq % QS;
           if (needq) {
-            if (!mbar_wait_spin(bar_qfull + t, nq & 1, wd)) return false;
+            if (!mbar_wait_spin_w(bar_qfull + qb, (nq / QS) & 1, wd)) return false;
             needq = false;
           }
-          if (!mbar_wait_spin(bar_kfull + (uu % KS), (uu / KS) & 1, wd)) return false;
-          const uint64_t qd = desc_adv(q_desc, t * L::kTile);
+          if (!mbar_wait_spin_w(bar_kfull + (uu % KS), (uu / KS) & 1, wd)) return false;
+          if (kSepP && ns >= 1) {  // the softmax has read S_t(previous) out of TMEM
+            if (!mbar_wait_spin_w(bar_sfree + t, (ns - 1) & 1, wd)) return false;
+            tc_fence_after();
+          }
+          ++ns;
+          const uint64_t qd = desc_adv(q_desc, qb * L::kTile);
           const uint64_t kd = desc_adv(k_desc, (uu % KS) * L::kTile);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-            mma_ss(tmem + t * 128, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + t * 128, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(bar_sfull + t);
+          mma_commit_w(bar_sfull + t);
           if (j == (t ? lastB : lastA)) {  // Q_t of this item is no longer needed
-            mma_commit(bar_qempty + t);
+            mma_commit_w(bar_qempty + qb);
             ++nq;
           }
           return true;
@@ -333,18 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           constexpr int t = decltype(slot)::value;
           int& npv = t ? npvB : npvA;
           int& loc = t ? locB : locA;
-          if (!mbar_wait_spin(bar_pfull + t, npv & 1, wd)) return false;
-          if (!mbar_wait_spin(bar_vfull + (uu % VS), (uu / VS) & 1, wd)) return false;
+          if (!mbar_wait_spin_w(bar_pfull + t, npv & 1, wd)) return false;
+          if (!mbar_wait_spin_w(bar_vfull + (uu % VS), (uu / VS) & 1, wd)) return false;
           tc_fence_after();
           const uint64_t vd = desc_adv(v_desc, (uu % VS) * L::kTile);
           const uint32_t acc0 = loc > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < kBlock / 16; ++kk) {
-            // A = P (bf16 pairs in the first 64 columns of S_t), B = V, MN-major.
-            mma_ts(tmem + L::kTO + t * D, tmem + t * 128 + kk * 8, desc_adv(vd, kk * 2048), kIdO,
+            // A = P_t (bf16 pairs, from TMEM), B = V, MN-major.
+            mma_ts_w(tmem + L::kTO + t * D, tmem + L::p_col(t) + kk * 8, desc_adv(vd, kk * 2048), kIdO,
                    kk > 0 ? 1u : acc0);
           }
-          mma_commit(bar_odone + t);
+          mma_commit_w(bar_odone + t);
           ++npv;
           ++loc;
           return true;
@@ -354,32 +378,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= it.uend) continue;
         if (it.tsA.has(j)) ok = issue_s(SlotA{}, u, j);
         if (ok && it.tsB.has(j)) ok = issue_s(SlotB{}, u, j);
-        if (ok) mma_commit(bar_kempty + (u % KS));
+        if (ok) mma_commit_w(bar_kempty + (u % KS));
         while (ok && j < it.uend) {
           int jn = j + 1;
           while (jn < it.uend && !it.tsA.has(jn) && !it.tsB.has(jn)) ++jn;
           const int un = u + 1;
-          // tile A: P_A(j) V_j, then S_A(j+1) over the columns P_A(j) just left
-          if (it.tsA.has(j)) ok = issue_pv(SlotA{}, u);
-          if (ok && jn < it.uend && it.tsA.has(jn)) ok = issue_s(SlotA{}, un, jn);
-          if (ok && it.tsB.has(j)) ok = issue_pv(SlotB{}, u);
-          if (ok) mma_commit(bar_vempty + (u % VS));
-          if (ok && jn < it.uend && it.tsB.has(jn)) ok = issue_s(SlotB{}, un, jn);
-          if (ok && jn < it.uend) mma_commit(bar_kempty + (un % KS));
+          if constexpr (kSepP) {
+            // S_t(j+1) as soon as the softmax has read S_t(j), so that it is
+            // ready when P_t(j) is; then P_A(j) V_j and P_B(j) V_j.
+            if (jn < it.uend) {
+              if (it.tsA.has(jn)) ok = issue_s(SlotA{}, un, jn);
+              if (ok && it.tsB.has(jn)) ok = issue_s(SlotB{}, un, jn);
+              if (ok) mma_commit_w(bar_kempty + (un % KS));
+            }
+            if (ok && it.tsA.has(j)) ok = issue_pv(SlotA{}, u);
+            if (ok && it.tsB.has(j)) ok = issue_pv(SlotB{}, u);
+            if (ok) mma_commit_w(bar_vempty + (u % VS));
+          } else {
+            // tile A: P_A(j) V_j, then S_A(j+1) over the columns P_A(j) just left
+            if (it.tsA.has(j)) ok = issue_pv(SlotA{}, u);
+            if (ok && jn < it.uend && it.tsA.has(jn)) ok = issue_s(SlotA{}, un, jn);
+            if (ok && it.tsB.has(j)) ok = issue_pv(SlotB{}, u);
+            if (ok) mma_commit_w(bar_vempty + (u % VS));
+            if (ok && jn < it.uend && it.tsB.has(jn)) ok = issue_s(SlotB{}, un, jn);
+            if (ok && jn < it.uend) mma_commit_w(bar_kempty + (un % KS));
+          }
           j = jn;
           u = un;
         }
       }
-      mma_commit(bar_final);
+      mma_commit_w(bar_final);
       mbar_wait_drain(bar_final, 0, wait_limit);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax (warps 0-7)
-    const int t = warp >> 2;              // which Q slot
-    const int r = threadIdx.x & 127;      // row within the tile == TMEM lane
+    const int t = (warp - kSoftWarp0) >> 2;  // which Q slot
+    const int r = (warp & 3) * 32 + lane;     // row within the tile == TMEM lane (quarter warp % 4)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = t * 128;
+    const uint32_t p_col = L::p_col(t);
     const uint32_t o_col = L::kTO + t * D;
     int ns = 0;  // S tiles of this slot consumed so far (sfull / pfull / odone phases)
     bool ok = true;
@@ -408,6 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < 4; ++c) reg_fence(rs[c]);
+        if constexpr (kSepP) {  // S_t may be overwritten by the next tile's S now
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sfree + t);
+        }
         float sv[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(rs[c >> 5][c & 31]);
@@ -446,16 +489,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           ps[c & 7] += p0 + p1;
         }
         const float tsum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        // P_t over the first 64 columns of S_t (its fp32 values are already in registers)
-        tmem_st32(lane_base + s_col, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st32(lane_base + s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
-        if (n >= 1 && __any_sync(0xffffffffu, grow)) {
-          // O must be quiescent (this item's previous P V done) before it is rescaled.
+        if (kSepP && n >= 1) {
+          // P_t's columns are free (and O quiescent) once this item's previous P V is done.
           if (!mbar_wait_warp(bar_odone + t, (ns - 1) & 1, wd)) {
             ok = false;
             break;
           }
           tc_fence_after();
+        }
+        // P_t in its own columns, or over the first 64 columns of S_t (whose
+        // fp32 values are already in registers)
+        tmem_st32(lane_base + p_col, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st32(lane_base + p_col + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        if (n >= 1 && __any_sync(0xffffffffu, grow)) {
+          // O must be quiescent (this item's previous P V done) before it is rescaled.
+          if (!kSepP) {
+            if (!mbar_wait_warp(bar_odone + t, (ns - 1) & 1, wd)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
 #pragma unroll
           for (int c0 = 0; c0 < D / 32; ++c0) {
             uint32_t o[32];
@@ -523,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
