@@ -107,9 +107,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def stop(self):
+    def stop(self, window=None):
+        """Median SM clock and throttle reasons over the samples taken inside
+        `window` (monotonic start, end), or over all samples."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -119,7 +121,9 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if window is not None and not (window[0] <= t <= window[1] + 0.25):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -131,8 +135,11 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+               "samples": len(sm), "reasons": sorted(reasons)}
+        if window is not None:
+            out["window"] = "1 s of untimed steps of the same workload, then the timed steps"
+        return out
 
 
 # --------------------------------------------------------------------------- our arm
@@ -184,26 +191,42 @@ class Step:
 KERNELS = ["fwd", "bwd_pre", "bwd_main", "dq_convert"]
 
 
-def time_steps(step: Step, steps: int, warmup: int, flush, backward=True):
-    """Returns per-kernel lists of milliseconds (K entries each)."""
+def time_steps(step: Step, steps: int, warmup: int, flush, backward=True, split=True,
+               soak_s: float = 0.0):
+    """Times `steps` steps (L2 flushed before each). split=False: one pair of
+    events around each whole step, so consecutive kernels overlap their
+    launches (programmatic dependent launch); returns {"step": [ms, ...]}.
+    split=True: an event between every two kernels (which stops that
+    overlap); returns per-kernel lists. soak_s: seconds of untimed steps run
+    right before the timed ones, so that clock samples see the GPU under load."""
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
-    n_ev = 5 if backward else 2
-    times = {k: [] for k in KERNELS[:n_ev - 1]}
+    n_ev = (5 if backward else 2) if split else 2
+    times = ({k: [] for k in KERNELS[:n_ev - 1]} if split else {"step": []})
 
     def one(record):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] if record else None
         if record:
             evs[0].record(stream)
         step.fwd(sp)
-        if record:
+        if record and split:
             evs[1].record(stream)
         if backward:
             for i, rc in enumerate(step.bwd_stages(sp)):
                 assert rc == 0, rc
-                if record:
+                if record and split:
                     evs[2 + i].record(stream)
+        if record and not split:
+            evs[1].record(stream)
         return evs
+
+    if soak_s > 0:
+        t_end = time.monotonic() + soak_s
+        while time.monotonic() < t_end:
+            for _ in range(20):
+                flush.zero_()
+                one(False)
+            torch.cuda.synchronize()
 
     for _ in range(warmup):
         one(False)
@@ -330,12 +353,19 @@ def run_ours(args, world, rank, local):
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    times = time_steps(step, args.steps, args.warmup, flush, backward=w.backward)
+    # timed region: K whole steps, events only around each step
+    t_region = [time.monotonic()]
+    whole = time_steps(step, args.steps, args.warmup, flush, backward=w.backward, split=False,
+                       soak_s=1.0)
+    t_region.append(time.monotonic())
     torch.cuda.synchronize()
     barrier(world)
-    per_kernel = {k: sum(v) / len(v) for k, v in times.items()}
-    ms_step = sum(per_kernel.values())
+    ms_step = sum(whole["step"]) / len(whole["step"])
     ms_step = max_over_ranks(world, ms_step)
+    # the same steps again with an event between kernels: per-kernel split and
+    # the dominant kernel's roofline
+    times = time_steps(step, args.steps, 3, flush, backward=w.backward, split=True)
+    per_kernel = {k: sum(v) / len(v) for k, v in times.items()}
     f_fwd, f_bwd = flops(w)
     step_flops = f_fwd + (f_bwd if w.backward else 0.0)
     value = world * step_flops / (ms_step * 1e-3) / 1e12
@@ -355,7 +385,7 @@ def run_ours(args, world, rank, local):
                     "traffic": ncu_traffic(dom, w.name)}
 
     e2e_ms, h2d, d2h = e2e(fa, step, max(3, args.steps // 4), 3) if w.backward else (None, 0, 0)
-    clk = clocks.stop()
+    clk = clocks.stop(window=tuple(t_region))
 
     out = {
         "metric": "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense BF16 tensor peak",
@@ -366,10 +396,13 @@ def run_ours(args, world, rank, local):
         "config": {"workload": f"{w.name}: {'causal' if w.causal else 'non-causal'} fwd+bwd, "
                                f"B={w.B} H={w.H} N={w.N} d={w.d}",
                    "pass": "fwd + bwd (preprocess, main, dQ convert)",
+                   "launch": "programmatic dependent launch between the four kernels",
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world} (independent (b,h) problems, no collective)"},
         "pct_of_bf16_peak": round(value / world / peak_tf, 4),
         "per_kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
+        "per_kernel_timing": "second pass of the same steps with an event between kernels "
+                             "(no launch overlap); ms_per_step is the whole-step timing",
         "fwd_tflops": round(f_fwd / (per_kernel["fwd"] * 1e-3) / 1e12, 2),
         "gpu_launches": args.steps * len(per_kernel),
         "roofline": roofline,

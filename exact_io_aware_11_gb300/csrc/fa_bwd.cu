@@ -105,6 +105,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       float* __restrict__ dq_acc, int BH, int N,
                                                       int Npad) {
   constexpr int kPer = D / 8;  // threads per row (8 elements = 16 bytes each)
+  grid_dep_wait();
+  grid_dep_launch();
   const long long total = static_cast<long long>(BH) * Npad * kPer;
   const long long total32 = (total + 31) & ~31LL;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -156,6 +158,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
                                                          __nv_bfloat16* __restrict__ dq, int BH,
                                                          int N, int Npad) {
   constexpr int kPer = D / 8;
+  grid_dep_wait();
+  grid_dep_launch();
   const long long total = static_cast<long long>(BH) * N * kPer;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
@@ -326,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
+  grid_dep_launch();
   const Watchdog wd{wait_limit, status, abort_flag};
 
   if (warp == 8) {
@@ -724,10 +730,9 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
   const int Npad = nt * kBlock;
   cudaError_t e = cudaSuccess;
   if (stages & kBwdStagePre) {
-    bwd_pre_kernel<D><<<grid_for(static_cast<long long>(BH) * Npad * (D / 8)), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse,
-        a.lse2, a.delta, a.dq_acc, BH, a.N, Npad);
-    e = cudaGetLastError();
+    e = launch_pdl(bwd_pre_kernel<D>, dim3(grid_for(static_cast<long long>(BH) * Npad * (D / 8))),
+                   dim3(256), 0, stream, a.o, a.dout, a.lse, a.lse2, a.delta, a.dq_acc, BH, a.N,
+                   Npad);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageMain) {
@@ -741,17 +746,14 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
     g.BH = BH;
     g.n_items = BH * nt;
     g.kv_len = a.kv_len;
-    kern<<<min(g.n_items, sm_count()), kThreads, L::kSmem, stream>>>(
-        a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, static_cast<__nv_bfloat16*>(a.dk),
-        static_cast<__nv_bfloat16*>(a.dv), a.lse2, a.delta, g, Npad, a.scale, a.status,
-        a.wait_limit);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(min(g.n_items, sm_count())), dim3(kThreads), L::kSmem, stream,
+                   a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g,
+                   Npad, a.scale, a.status, a.wait_limit);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageConvert) {
-    dq_convert_kernel<D><<<grid_for(static_cast<long long>(BH) * a.N * (D / 8)), 256, 0, stream>>>(
-        a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), BH, a.N, Npad);
-    e = cudaGetLastError();
+    e = launch_pdl(dq_convert_kernel<D>, dim3(grid_for(static_cast<long long>(BH) * a.N * (D / 8))),
+                   dim3(256), 0, stream, a.dq_acc, a.dq, BH, a.N, Npad);
   }
   return e;
 }

@@ -233,6 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
+  grid_dep_launch();
   const Watchdog wd{wait_limit, status, abort_flag};
 
   if (warp == kLoadWarp) {
@@ -599,9 +601,8 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   g.block_mask = a.block_mask;
   const int grid = min(g.n_items, sm_count());
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  kern<<<grid, kThreads, L::kSmem, stream>>>(a.tm_q, a.tm_k, a.tm_v, static_cast<__nv_bfloat16*>(a.o),
-                                             a.lse, g, scale_log2, a.status, a.wait_limit);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
+                    a.o, a.lse, g, scale_log2, a.status, a.wait_limit);
 }
 
 }  // namespace

@@ -57,6 +57,28 @@ BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
+// Launches `kern` with programmatic dependent launch allowed: the grid may be
+// set up while the previous kernel on the stream is still running, and every
+// kernel of this library waits (griddepcontrol.wait) for its predecessor's
+// completion before it touches global memory, then lets its own successor be
+// set up (griddepcontrol.launch_dependents). This hides the launch gap between
+// the kernels of a forward + backward pass.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
 // Backward stages (bit set): preprocess, main kernel, dQ conversion.
 constexpr int kBwdStagePre = 1, kBwdStageMain = 2, kBwdStageConvert = 4, kBwdStageAll = 7;

@@ -45,6 +45,17 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Waits until the grids this one depends on (the previous kernel on the
+// stream, when launched with programmatic dependent launch) have completed
+// and their memory is visible; a no-op otherwise.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allows the next kernel on the stream to be set up now; it still waits for
+// this grid's completion before it reads anything.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -129,14 +140,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait that polls with the non-blocking test_wait instead of letting
-// the hardware suspend the thread: for a single thread on the critical path
-// (the MMA issuer), which must react to a phase change at once.
+// Bounded wait for the MMA issuer: one non-blocking test_wait first (the
+// phase has usually completed already), then try_wait, which lets the
+// hardware park the warp instead of spinning; a spinning issuer warp takes
+// issue slots from the compute warps that share its sub-partition.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_test_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*wd.abort) return false;
     if (clock64() - t0 > wd.limit) {
       watchdog_fire(wd.status, wd.abort);

@@ -119,3 +119,42 @@ def test_bwd_many_items_per_cta(fa, causal, d):
     dk, dv = f64(grads[1]), f64(grads[2])
     for b, L in enumerate(kv.tolist()):
         assert np.all(dk[b, :, L:] == 0) and np.all(dv[b, :, L:] == 0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_kv_len_zero_gives_zero_grads(fa, d, causal):
+    # A batch with no valid key: its rows see nothing, so every gradient of
+    # that batch is exactly zero (no key tile contributes to its dQ tiles).
+    kv = torch.tensor([0, 5, 300], dtype=torch.int32)
+    w, x = generic(len(kv), 2, 300, d, causal, seed=21)
+    g = run(fa, x, causal, w.scale, kv)
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, causal=causal,
+                          kv_len=kv.numpy())
+    check_grads(g, ref, f"kv_len 0 d={d} causal={causal}")
+    for t in g:
+        assert torch.count_nonzero(t[0]) == 0
+
+
+def test_bwd_stages_match_fused_call(fa):
+    # fa_bwd_preprocess, fa_bwd_main, fa_bwd_dq_convert on one stream is fa_bwd.
+    import ctypes
+    w, x = generic(2, 3, 700, 64, True, seed=22)
+    q, k, v, do = cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["dout"])
+    o, lse = fa.forward(q, k, v, causal=True, scale=w.scale)
+    ref = fa.backward(q, k, v, o, do, lse, causal=True, scale=w.scale)
+    need = fa.bwd_workspace_bytes(2, 3, 700, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    L = fa.lib()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert L.fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), lse.data_ptr(), 2, 3, 700, 64,
+                               ws.data_ptr(), need, s) == 0
+    assert L.fa_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), dk.data_ptr(),
+                         dv.data_ptr(), 2, 3, 700, 64, 1, w.scale, None, ws.data_ptr(), need,
+                         s) == 0
+    assert L.fa_bwd_dq_convert(dq.data_ptr(), 2, 3, 700, 64, ws.data_ptr(), need, s) == 0
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+    assert torch.allclose(dq.float(), ref[0].float(), rtol=0, atol=1e-2)
