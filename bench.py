@@ -51,11 +51,12 @@ def peaks():
 
 
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by kernel and
-# workload, valid only while the kernel's source is unchanged (first 16 hex
-# digits of its SHA-256 when it was captured; see profiles/).
+# workload, valid only while the kernel's sources are unchanged (first 16 hex
+# digits of the SHA-256 of its .cu file followed by the shared PTX header when
+# it was captured; see profiles/).
 NCU_TRAFFIC = {
-    ("bwd_main", "gpt2_small"): (85_147_904, "fa_bwd.cu", "2ecfa0c73e81fa95"),
-    ("fwd", "gpt2_small"): (37_917_952, "fa_fwd.cu", "cc305a1f9505d983"),
+    ("bwd_main", "gpt2_small"): (81_097_728, "fa_bwd.cu", "c253d35dc8b4d989"),
+    ("fwd", "gpt2_small"): (37_839_360, "fa_fwd.cu", "36f0d284e83747cb"),
 }
 
 
@@ -65,12 +66,15 @@ def ncu_traffic(kernel: str, workload: str):
     if entry is None:
         return None
     nbytes, src, digest = entry
-    path = os.path.join(ROOT, "exact_io_aware_11_gb300", "csrc", src)
+    csrc = os.path.join(ROOT, "exact_io_aware_11_gb300", "csrc")
+    h = hashlib.sha256()
     try:
-        with open(path, "rb") as f:
-            now = hashlib.sha256(f.read()).hexdigest()[:16]
+        for name in (src, "fa_ptx.cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
     except OSError:
         return None
+    now = h.hexdigest()[:16]
     return nbytes if now == digest else None
 
 
@@ -356,7 +360,7 @@ def run_ours(args, world, rank, local):
     # timed region: K whole steps, events only around each step
     t_region = [time.monotonic()]
     whole = time_steps(step, args.steps, args.warmup, flush, backward=w.backward, split=False,
-                       soak_s=1.0)
+                       soak_s=args.soak)
     t_region.append(time.monotonic())
     torch.cuda.synchronize()
     barrier(world)
@@ -484,6 +488,8 @@ def main():
     ap.add_argument("--workload", default="gpt2_small", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of untimed steps right before the timed ones (clock samples)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
