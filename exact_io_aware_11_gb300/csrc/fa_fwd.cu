@@ -53,11 +53,15 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
-// Warp roles. The MMA issuer is warp 0: among eligible warps the scheduler
-// favours lower warp ids, and the issuer competes for issue slots with two
-// softmax warps on its sub-partition.
-constexpr int kMmaWarp = 0, kLoadWarp = 1, kSoftWarp0 = 2;
+// Warp roles: warp 0 issues MMAs (at d = 64 for Q tile slot A only, warp 2
+// for slot B), warp 1 issues TMA copies, then four softmax warps per slot.
+constexpr int kMmaWarp = 0, kLoadWarp = 1;
+template <int D>
+struct FwdWarps {
+  static constexpr int kMmaB = (D == 64) ? 2 : -1;  // second MMA issuer (d = 64)
+  static constexpr int kSoft0 = (D == 64) ? 3 : 2;  // first softmax warp
+  static constexpr int kThreads = (kSoft0 + 8) * 32;
+};
 constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled chunk (64 bf16 cols)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
@@ -174,7 +178,7 @@ __device__ __forceinline__ int item_of(const FwdGrid& g, int r) {
 }
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                float* __restrict__ lse_out, FwdGrid g, float scale_log2, int* status,
@@ -195,9 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_pfull = bars + 22;   // [2]
   uint64_t* bar_odone = bars + 24;   // [2]
   uint64_t* bar_sfree = bars + 26;   // [2] S_t read out of TMEM (separate-P layout)
-  uint64_t* bar_final = bars + 28;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
-  int* abort_flag = reinterpret_cast<int*>(bars + 30);
+  uint64_t* bar_final = bars + 28;   // [2] one per MMA issuer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
+  int* abort_flag = reinterpret_cast<int*>(bars + 31);
+  constexpr int kMmaB = FwdWarps<D>::kMmaB, kSoft0 = FwdWarps<D>::kSoft0;
+  constexpr int kIssuers = kSepP ? 2 : 1;  // arrivals that release a K or V ring slot
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -215,13 +221,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < KS; ++s) {
       mbar_init(bar_kfull + s, 1);
-      mbar_init(bar_kempty + s, 1);
+      mbar_init(bar_kempty + s, kIssuers);
     }
     for (int s = 0; s < VS; ++s) {
       mbar_init(bar_vfull + s, 1);
-      mbar_init(bar_vempty + s, 1);
+      mbar_init(bar_vempty + s, kIssuers);
     }
     mbar_init(bar_final, 1);
+    mbar_init(bar_final + 1, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -293,15 +300,142 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bar_vfull + (t % VS), (t / VS) & 1, wait_limit);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer (whole warp)
-    // The issuer sits on the critical path between the two softmax
-    // warpgroups. The warp runs converged and an elected lane issues each
-    // tcgen05.mma / commit; it polls the barriers (test_wait) and places a
-    // tcgen05 fence only after waiting on another thread's TMEM access (P_t
-    // written by tcgen05.st; S_t read by tcgen05.ld before S_t(j+1) overwrites
-    // it).
-    {
+  } else if (warp == kMmaWarp || warp == kMmaB) {
+    // ------------------------------------------------------------ MMA issuers (whole warps)
+    // An issuer sits on the critical path between the softmax warpgroups. The
+    // warp runs converged and an elected lane issues each tcgen05.mma /
+    // commit; it polls the barriers and places a tcgen05 fence only after
+    // waiting on another thread's TMEM access (P_t written by tcgen05.st; S_t
+    // read by tcgen05.ld before S_t(j+1) overwrites it).
+    if constexpr (kSepP) {
+      // d = 64: one issuer per Q tile slot X, each walking every K/V tile of
+      // its items. Both release each K and V ring slot (count 2): with an MMA
+      // commit when slot X used the tile, else with a plain arrive once the
+      // tile is known to be loaded, which keeps the ring's phases in order.
+      const int X = (warp == kMmaWarp) ? 0 : 1;
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
+      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);     // K-major
+      const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
+      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
+      const uint32_t s_tm = tmem + X * 128, o_tm = tmem + L::kTO + X * D;
+      const uint32_t p_tm = tmem + L::p_col(X);
+      uint64_t* my_sfull = bar_sfull + X;
+      uint64_t* my_sfree = bar_sfree + X;
+      uint64_t* my_pfull = bar_pfull + X;
+      uint64_t* my_odone = bar_odone + X;
+      int npv = 0, nq = 0, ns = 0;  // P V MMAs, Q tiles, S tiles of this slot so far
+      int u = 0;                    // position in the K/V rings
+      int k_ready = -1, v_ready = -1;  // ring positions already seen loaded
+      bool ok = true;
+      auto k_wait = [&](int uu) -> bool {
+        if (uu == k_ready) return true;
+        if (!mbar_wait_spin_w(bar_kfull + (uu % KS), (uu / KS) & 1, wd)) return false;
+        k_ready = uu;
+        return true;
+      };
+      auto v_wait = [&](int uu) -> bool {
+        if (uu == v_ready) return true;
+        if (!mbar_wait_spin_w(bar_vfull + (uu % VS), (uu / VS) & 1, wd)) return false;
+        v_ready = uu;
+        return true;
+      };
+      for (int r = 0; ok; ++r) {
+        const int k = item_of(g, r);
+        if (k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, k);
+        const TileSet my = X ? it.tsB : it.tsA;
+        const int last = my.last();
+        bool needq = last >= 0;
+        int loc = 0;  // P V MMAs of this item
+        const int qb = X * QS + nq % QS;
+        auto issue_s = [&](int uu, int j) -> bool {
+          if (needq) {
+            if (!mbar_wait_spin_w(bar_qfull + qb, (nq / QS) & 1, wd)) return false;
+            needq = false;
+          }
+          if (!k_wait(uu)) return false;
+          if (ns >= 1) {  // the softmax has read S_X(previous) out of TMEM
+            if (!mbar_wait_spin_w(my_sfree, (ns - 1) & 1, wd)) return false;
+            tc_fence_after();
+          }
+          ++ns;
+          const uint64_t qd = desc_adv(q_desc, qb * L::kTile);
+          const uint64_t kd = desc_adv(k_desc, (uu % KS) * L::kTile);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            mma_ss_w(s_tm, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_w(my_sfull);
+          if (j == last) {  // Q_X of this item is no longer needed
+            mma_commit_w(bar_qempty + qb);
+            ++nq;
+          }
+          return true;
+        };
+        auto issue_pv = [&](int uu) -> bool {
+          if (!mbar_wait_spin_w(my_pfull, npv & 1, wd)) return false;
+          if (!v_wait(uu)) return false;
+          tc_fence_after();
+          const uint64_t vd = desc_adv(v_desc, (uu % VS) * L::kTile);
+          const uint32_t acc0 = loc > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < kBlock / 16; ++kk)
+            mma_ts_w(o_tm, p_tm + kk * 8, desc_adv(vd, kk * 2048), kIdO, kk > 0 ? 1u : acc0);
+          mma_commit_w(my_odone);
+          ++npv;
+          ++loc;
+          return true;
+        };
+        auto release_k = [&](int uu, bool used) -> bool {
+          if (used) {
+            mma_commit_w(bar_kempty + (uu % KS));
+            return true;
+          }
+          if (!k_wait(uu)) return false;
+          mbar_arrive_w(bar_kempty + (uu % KS));
+          return true;
+        };
+        auto release_v = [&](int uu, bool used) -> bool {
+          if (used) {
+            mma_commit_w(bar_vempty + (uu % VS));
+            return true;
+          }
+          if (!v_wait(uu)) return false;
+          mbar_arrive_w(bar_vempty + (uu % VS));
+          return true;
+        };
+        int j = 0;
+        while (j < it.uend && !it.tsA.has(j) && !it.tsB.has(j)) ++j;
+        if (j >= it.uend) continue;
+        {
+          const bool h = my.has(j);
+          if (h) ok = issue_s(u, j);
+          if (ok) ok = release_k(u, h);
+        }
+        while (ok && j < it.uend) {
+          int jn = j + 1;
+          while (jn < it.uend && !it.tsA.has(jn) && !it.tsB.has(jn)) ++jn;
+          const int un = u + 1;
+          // S_X(j+1) as soon as the softmax has read S_X(j), then P_X(j) V_j
+          if (jn < it.uend) {
+            const bool h = my.has(jn);
+            if (h) ok = issue_s(un, jn);
+            if (ok) ok = release_k(un, h);
+          }
+          if (ok) {
+            const bool h = my.has(j);
+            if (h) ok = issue_pv(u);
+            if (ok) ok = release_v(u, h);
+          }
+          j = jn;
+          u = un;
+        }
+      }
+      mma_commit_w(bar_final + X);
+      mbar_wait_drain(bar_final + X, 0, wait_limit);
+    } else {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
       // Descriptors built once; per MMA only a compile-time offset is added.
@@ -415,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax (warps 0-7)
-    const int t = (warp - kSoftWarp0) >> 2;  // which Q slot
+    const int t = (warp - kSoft0) >> 2;  // which Q slot
     const int r = (warp & 3) * 32 + lane;     // row within the tile == TMEM lane (quarter warp % 4)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const uint32_t s_col = t * 128;
@@ -479,18 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new = grow ? tmax : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = grow ? ex2(m - m_use) : 1.f;
-        uint32_t pk[64];
-        float ps[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ps[i] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2(fmaf(sv[2 * c], scale_log2, -m_use));
-          const float p1 = ex2(fmaf(sv[2 * c + 1], scale_log2, -m_use));
-          pk[c] = pack_bf16(p0, p1);
-          ps[c & 7] += p0 + p1;
-        }
-        const float tsum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         if (kSepP && n >= 1) {
           // P_t's columns are free (and O quiescent) once this item's previous P V is done.
           if (!mbar_wait_warp(bar_odone + t, (ns - 1) & 1, wd)) {
@@ -499,10 +621,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
         }
-        // P_t in its own columns, or over the first 64 columns of S_t (whose
-        // fp32 values are already in registers)
-        tmem_st32(lane_base + p_col, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st32(lane_base + p_col + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        // P_t (bf16 pairs) goes to TMEM 16 columns at a time as soon as it is
+        // formed -- in its own columns, or over the first 64 columns of S_t,
+        // whose fp32 values are already in registers -- so that few packed
+        // words are live at once.
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float p0 = ex2(fmaf(sv[2 * (c0 + c)], scale_log2, -m_use));
+            const float p1 = ex2(fmaf(sv[2 * (c0 + c) + 1], scale_log2, -m_use));
+            pk[c] = pack_bf16(p0, p1);
+            ps[c & 3] += p0 + p1;
+          }
+          tmem_st16(lane_base + p_col + c0, pk);
+        }
+        const float tsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         if (n >= 1 && __any_sync(0xffffffffu, grow)) {
           // O must be quiescent (this item's previous P V done) before it is rescaled.
           if (!kSepP) {
@@ -601,7 +737,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   g.block_mask = a.block_mask;
   const int grid = min(g.n_items, sm_count());
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
+  return launch_pdl(kern, dim3(grid), dim3(FwdWarps<D>::kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
                     a.o, a.lse, g, scale_log2, a.status, a.wait_limit);
 }
 

@@ -374,6 +374,15 @@ __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
       : "memory");
 }
 
+// Plain (immediate) arrive by one elected lane of a converged warp.
+__device__ __forceinline__ void mbar_arrive_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n\t}" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
