@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       int n = 0;            // tiles of this item
       for (int j = 0; j < my.end; ++j) {
         if (!my.has(j)) continue;
-        if (!mbar_wait_warp(bar_sfull + t, ns & 1, wd)) {
+        if (!mbar_wait_warp<true>(bar_sfull + t, ns & 1, wd)) {
           ok = false;
           break;
         }
@@ -615,7 +615,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         const float alpha = grow ? ex2(m - m_use) : 1.f;
         if (kSepP && n >= 1) {
           // P_t's columns are free (and O quiescent) once this item's previous P V is done.
-          if (!mbar_wait_warp(bar_odone + t, (ns - 1) & 1, wd)) {
+          if (!mbar_wait_warp<true>(bar_odone + t, (ns - 1) & 1, wd)) {
             ok = false;
             break;
           }
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         if (n >= 1 && __any_sync(0xffffffffu, grow)) {
           // O must be quiescent (this item's previous P V done) before it is rescaled.
           if (!kSepP) {
-            if (!mbar_wait_warp(bar_odone + t, (ns - 1) & 1, wd)) {
+            if (!mbar_wait_warp<true>(bar_odone + t, (ns - 1) & 1, wd)) {
               ok = false;
               break;
             }
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       // arrives, i.e. after these loads.
       bool have = n > 0;
       if (have) {
-        if (!mbar_wait_warp(bar_odone + t, (ns - 1) & 1, wd)) {
+        if (!mbar_wait_warp<true>(bar_odone + t, (ns - 1) & 1, wd)) {
           ok = false;
           break;
         }

@@ -102,9 +102,16 @@ static __device__ __noinline__ void watchdog_fire(int* status, volatile int* abo
   *abort = 1;
   atomicCAS(status, FA_OK, FA_ERR_DEVICE_TIMEOUT);
 }
+// Same, inlined: for waits of threads that hold many live registers (the
+// forward softmax), where the call's register saves cost more than the code.
+static __device__ __forceinline__ void watchdog_fire_inline(int* status, volatile int* abort) {
+  *abort = 1;
+  atomicCAS(status, FA_OK, FA_ERR_DEVICE_TIMEOUT);
+}
 
 // Waits for the phase with the given parity to complete. Returns false if the
 // CTA is aborting or the budget ran out (then the abort flag is raised).
+template <bool kInlineFire = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
@@ -112,7 +119,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (mbar_try_wait(bar, parity)) return true;
     if (*wd.abort) return false;
     if (clock64() - t0 > wd.limit) {
-      watchdog_fire(wd.status, wd.abort);
+      if (kInlineFire)
+        watchdog_fire_inline(wd.status, wd.abort);
+      else
+        watchdog_fire(wd.status, wd.abort);
       return false;
     }
   }
@@ -166,8 +176,9 @@ __device__ __forceinline__ bool mbar_wait_spin_w(uint64_t* bar, uint32_t parity,
 }
 
 // Warp-uniform wait: every lane waits, lane 0's verdict is broadcast.
+template <bool kInlineFire = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
-  bool ok = mbar_wait(bar, parity, wd);
+  bool ok = mbar_wait<kInlineFire>(bar, parity, wd);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
