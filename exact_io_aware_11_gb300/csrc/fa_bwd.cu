@@ -289,6 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_final = bars + 22;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
   int* abort_flag = reinterpret_cast<int*>(bars + 24);
+  uint64_t* bar_dpfree = bars + 25;   // dP^T read out of TMEM (d = 64)
+  // d = 64: dQ has TMEM columns of its own, so dP^T of the next Q tile can be
+  // issued as soon as the compute warps have read dP^T of this one, ahead of
+  // this tile's dK and dQ MMAs in the in-order tensor pipe.
+  constexpr bool kEarlyDP = (D == 64);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -319,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_dvempty, 4);
     mbar_init(bar_dkempty, 4);
     mbar_init(bar_final, 1);
+    mbar_init(bar_dpfree, 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -462,6 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with a single K/V stage it must wait until this item's dQ is issued.
         const bool hoist = nx.valid && (KVS > 1 || !last);
         if (hoist && !((nx.it > 0 || kv_ready(nx)) && issue_s(nx))) { ok = false; break; }
+        if (kEarlyDP && nx.valid) {  // hoist is true here: KVS > 1 at d = 64
+          if (!mbar_wait_spin_w(bar_dpfree, gq & 1, wd)) { ok = false; break; }
+          tc_fence_after();
+          if (!issue_dp(nx)) { ok = false; break; }
+        }
         if (!mbar_wait_spin_w(bar_dsready, gq & 1, wd)) { ok = false; break; }
         if (D == 64 && gq >= 1 && !mbar_wait_spin_w(bar_dqfree, (gq - 1) & 1, wd)) { ok = false; break; }
         if (first && cur.t >= 1 && !mbar_wait_spin_w(bar_dkempty, (cur.t - 1) & 1, wd)) { ok = false; break; }
@@ -490,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_spin_w(bar_dqfree, gq & 1, wd)) { ok = false; break; }
             tc_fence_after();
           }
-          if (!issue_dp(nx)) { ok = false; break; }
+          if (!kEarlyDP && !issue_dp(nx)) { ok = false; break; }
         }
         cur = nx;
       }
@@ -669,6 +680,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_fence(rr[0]);
         reg_fence(rr[1]);
+        if constexpr (kEarlyDP) {  // dP^T may be overwritten by the next tile's now
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dpfree);
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int q0 = u * 8;
