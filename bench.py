@@ -181,6 +181,15 @@ class Step:
 
     def bwd_stages(self, stream):
         w, L = self.w, self.L
+        if self.mask is not None:  # block-sparse: one call runs all three kernels
+            yield L.fa_blocksparse_bwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                       self.o.data_ptr(), self.do.data_ptr(), self.lse.data_ptr(),
+                                       self.dq.data_ptr(), self.dk.data_ptr(), self.dv.data_ptr(),
+                                       w.B, w.H, w.N, w.d, w.scale, self.mask.data_ptr(), 128,
+                                       self.ws.data_ptr(), self.ws_bytes, stream)
+            yield 0
+            yield 0
+            return
         kv = None if self.kv is None else self.kv.data_ptr()
         yield L.fa_bwd_preprocess(self.o.data_ptr(), self.do.data_ptr(), self.lse.data_ptr(),
                                   w.B, w.H, w.N, w.d, self.ws.data_ptr(), self.ws_bytes, stream)
@@ -432,8 +441,9 @@ def sweep(fa, dev, flush, pk):
         st = Step(fa, w, 0, dev)
         t = time_steps(st, 10, 3, flush, backward=w.backward)
         f_fwd, f_bwd = flops(w)
-        if w.sparse:
+        if w.sparse:  # effective work: kept blocks only
             f_fwd = 4.0 * w.B * w.H * w.d * 128 * 128 * int(st.host["block_mask"].sum())
+            f_bwd = 2.5 * f_fwd
         r = {"fwd_ms": round(statistics.median(t["fwd"]), 4),
              "fwd_tflops": round(f_fwd / (statistics.median(t["fwd"]) * 1e-3) / 1e12, 2)}
         r["fwd_pct_peak"] = round(r["fwd_tflops"] / pk["bf16_tflops"], 4)
@@ -443,7 +453,10 @@ def sweep(fa, dev, flush, pk):
             r["bwd_ms"] = round(mb, 4)
             r["bwd_tflops"] = round(f_bwd / (mb * 1e-3) / 1e12, 2)
             r["bwd_pct_peak"] = round(r["bwd_tflops"] / pk["bf16_tflops"], 4)
-            r["bwd_main_ms"] = round(statistics.median(t["bwd_main"]), 4)
+            if w.sparse:
+                r["bwd_timing"] = "one fa_blocksparse_bwd call (preprocess, main, dQ convert)"
+            else:
+                r["bwd_main_ms"] = round(statistics.median(t["bwd_main"]), 4)
         res[name] = r
         del st
         torch.cuda.empty_cache()

@@ -32,6 +32,7 @@ SIGNATURES = {
     "fa_bwd_main": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, ctypes.c_size_t,
                          _P]),
     "fa_bwd_dq_convert": (_I, [_P, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
+    "fa_blocksparse_bwd": (_I, [_P] * 9 + [_I, _I, _I, _I, _F, _P, _I, _P, ctypes.c_size_t, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P]),
     "fa_blocksparse_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P]),
     "fa_device_status": (_I, []),
@@ -153,6 +154,31 @@ def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = 
                       int(bool(causal)), scale, _ptr(kv_len), ws.data_ptr(), ws.numel(),
                       _stream_ptr(stream))
     _raise(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def blocksparse_backward(q, k, v, o, dout, lse, block_mask, scale: float | None = None,
+                         block_size: int = 128, workspace=None, dq=None, dk=None, dv=None,
+                         stream=None):
+    """dQ, dK, dV of the block-sparse forward (fa_blocksparse_bwd)."""
+    _check_qkv(q, k, v, o, dout)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if block_mask.dtype != torch.uint8 or not block_mask.is_cuda or not block_mask.is_contiguous():
+        raise ValueError("block_mask must be a contiguous CUDA uint8 tensor [nb, nb]")
+    nb = (N + block_size - 1) // block_size
+    if tuple(block_mask.shape) != (nb, nb):
+        raise ValueError(f"block_mask must have shape ({nb}, {nb})")
+    need = bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    rc = lib().fa_blocksparse_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), B, H, N, d, scale, block_mask.data_ptr(),
+                                  int(block_size), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    _raise(rc, "fa_blocksparse_bwd")
     return dq, dk, dv
 
 

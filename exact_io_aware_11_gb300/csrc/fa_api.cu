@@ -176,7 +176,8 @@ struct BwdPtrs {
 // Validates and launches the requested backward stages. Pointers a stage does
 // not use may be NULL; every pointer a stage uses must be non-NULL.
 int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int causal, float scale,
-               const int32_t* kv_len, size_t workspace_bytes, cudaStream_t stream) {
+               const int32_t* kv_len, size_t workspace_bytes, cudaStream_t stream,
+               const uint8_t* block_mask = nullptr) {
   int st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
   const bool pre = stages & kBwdStagePre, mainst = stages & kBwdStageMain,
@@ -233,6 +234,7 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
   a.causal = causal;
   a.scale = scale;
   a.kv_len = kv_len;
+  a.block_mask = block_mask;
   a.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
   a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   a.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
@@ -303,6 +305,17 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            struct CUstream_st* stream) {
   const BwdPtrs p{q, k, v, o, dout, lse, dq, dk, dv, workspace};
   return bwd_common(kBwdStageAll, p, B, H, N, d, causal, scale, kv_len, workspace_bytes, stream);
+}
+
+int fa_blocksparse_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H, int N, int d, float scale, const uint8_t* block_mask, int block_size,
+                       void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  if (block_mask == nullptr) return FA_ERR_INVALID_ARG;
+  if (block_size != kBlock) return FA_ERR_UNSUPPORTED;
+  const BwdPtrs p{q, k, v, o, dout, lse, dq, dk, dv, workspace};
+  return bwd_common(kBwdStageAll, p, B, H, N, d, 0, scale, nullptr, workspace_bytes, stream,
+                    block_mask);
 }
 
 int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N,

@@ -186,16 +186,20 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 struct BwdGrid {
   int H, N, nt, BH, n_items;
   const int32_t* kv_len;
+  const uint8_t* mask;  // block-sparse: uint8 [nt][nt], nonzero = (query tile, key tile) kept
 };
 
 struct BwdItem {
-  int bh, j, i0, n_iter, kv_bound;
+  int bh, j, i0, n_iter, kv_bound;  // i0: first query tile met (the rest follow bwd_next_row)
 };
+
+template <bool SPARSE>
+__device__ __forceinline__ int bwd_next_row(const BwdGrid& g, int j, int i);
 
 // Item k. Causal items are ordered heaviest first (key tile j meets nt - j
 // query tiles); otherwise a head's key tiles are consecutive, so that CTAs
 // running at the same time stream the same Q and dO tiles through L2.
-template <bool CAUSAL>
+template <bool CAUSAL, bool SPARSE = false>
 __device__ __forceinline__ BwdItem make_bwd_item(const BwdGrid& g, int k) {
   BwdItem x;
   if (CAUSAL) {
@@ -209,7 +213,23 @@ __device__ __forceinline__ BwdItem make_bwd_item(const BwdGrid& g, int k) {
   if (g.kv_len != nullptr) x.kv_bound = min(g.N, max(0, g.kv_len[x.bh / g.H]));
   x.i0 = CAUSAL ? x.j : 0;
   x.n_iter = x.j * kBlock < x.kv_bound ? g.nt - x.i0 : 0;
+  if constexpr (SPARSE) {  // the query tiles whose mask row keeps key tile j
+    int n = 0;
+    for (int i = 0; i < g.nt; ++i) n += g.mask[static_cast<size_t>(i) * g.nt + x.j] != 0;
+    x.n_iter = n;
+    x.i0 = bwd_next_row<true>(g, x.j, 0);
+  }
   return x;
+}
+
+// The first query tile >= i that meets key tile j: i itself unless a block
+// mask says otherwise (nt if there is none).
+template <bool SPARSE>
+__device__ __forceinline__ int bwd_next_row(const BwdGrid& g, int j, int i) {
+  if constexpr (SPARSE) {
+    while (i < g.nt && g.mask[static_cast<size_t>(i) * g.nt + j] == 0) ++i;
+  }
+  return i;
 }
 
 // The r-th item of this CTA: a snake over the item list; -1 when there is none.
@@ -223,7 +243,7 @@ __device__ __forceinline__ int bwd_item_of(const BwdGrid& g, int r) {
 // Position of the MMA issuer in this CTA's flattened sequence of iterations:
 // iteration `it` of `n` of the t-th item that has iterations, the g-th
 // iteration overall (ring slots and barrier phases follow t and g).
-template <bool CAUSAL>
+template <bool CAUSAL, bool SPARSE>
 struct BwdCursor {
   int r = 0, it = 0, n = 0, t = 0, g = 0;
   bool valid = false;
@@ -234,7 +254,7 @@ struct BwdCursor {
         valid = false;
         return;
       }
-      const int n_iter = make_bwd_item<CAUSAL>(G, k).n_iter;
+      const int n_iter = make_bwd_item<CAUSAL, SPARSE>(G, k).n_iter;
       if (n_iter > 0) {
         n = n_iter;
         it = 0;
@@ -257,7 +277,7 @@ struct BwdCursor {
 // items, K/V of the next item are prefetched when shared memory holds two
 // stages (d = 64), and dK/dV are written from TMEM by the dQ drain warps while
 // the compute warps already form P of the next item.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -353,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; ok; ++r) {
         const int k = bwd_item_of(grid, r);
         if (k < 0) break;
-        const BwdItem x = make_bwd_item<CAUSAL>(grid, k);
+        const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
         if (x.n_iter == 0) continue;
         const int kvs = t % KVS;
         if (t >= KVS && !mbar_wait(bar_kvempty + kvs, ((t / KVS) - 1) & 1, wd)) break;
@@ -364,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(kv + L::kTile + c * kChunk, &tm_v, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh);
         }
         ++t;
-        for (int it = 0; it < x.n_iter; ++it) {
-          const int gq = q_issued, i = x.i0 + it, qs = gq % QS, ds = gq % DS;
+        for (int it = 0, i = x.i0; it < x.n_iter; ++it, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
+          const int gq = q_issued, qs = gq % QS, ds = gq % DS;
           if (gq >= QS && !mbar_wait(bar_qempty + qs, ((gq / QS) - 1) & 1, wd)) { ok = false; break; }
           mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
           for (int c = 0; c < L::kChunks; ++c)
@@ -413,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + L::kDO), kChunk, 1024);
       const uint64_t ds_kmaj = sdesc_sw128(smem_u32(smem + L::kDSb), 16, 1024);
       const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + L::kDSb), kChunk, 1024);
-      using Cur = BwdCursor<CAUSAL>;
+      using Cur = BwdCursor<CAUSAL, SPARSE>;
       auto kv_ready = [&](const Cur& c) -> bool {
         return mbar_wait_spin_w(bar_kvfull + (c.t % KVS), (c.t / KVS) & 1, wd);
       };
@@ -523,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; ok; ++r) {
       const int k = bwd_item_of(grid, r);
       if (k < 0) break;
-      const BwdItem x = make_bwd_item<CAUSAL>(grid, k);
+      const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
       const int key = x.j * kBlock + row;
       const size_t out_off = (static_cast<size_t>(x.bh) * N + key) * D;
       if (x.n_iter == 0) {  // no valid key in this tile: zero gradients
@@ -538,8 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      for (int it = 0; it < x.n_iter; ++it, ++gq) {
-        const int i = x.i0 + it;
+      for (int it = 0, i = x.i0; it < x.n_iter; ++it, ++gq, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
         if (!mbar_wait_warp(bar_dqfull, gq & 1, wd)) { ok = false; break; }
         tc_fence_after();
         uint32_t v[D / 32][32];
@@ -629,11 +648,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; ok; ++r) {
       const int k = bwd_item_of(grid, r);
       if (k < 0) break;
-      const BwdItem x = make_bwd_item<CAUSAL>(grid, k);
+      const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
       const bool key_live = x.j * kBlock + kr < x.kv_bound;
       for (int it = 0; it < x.n_iter; ++it, ++gq) {
         const int s = gq % QS;
-        const int i = x.i0 + it;
+        const int i = x.i0 + it;  // used only for the causal diagonal (dense)
         const float* st_lse = reinterpret_cast<const float*>(smem + L::kStat + s * 1024) + qc0;
         const float* st_delta = st_lse + 128;
         if (!mbar_wait_warp(bar_qfull + s, (gq / QS) & 1, wd)) { ok = false; break; }
@@ -752,7 +771,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageMain) {
-    auto kern = bwd_main_kernel<D, CAUSAL>;
+    auto kern = (!CAUSAL && a.block_mask != nullptr) ? bwd_main_kernel<D, false, true>
+                                                     : bwd_main_kernel<D, CAUSAL, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
     if (e != cudaSuccess) return e;
     BwdGrid g;
@@ -762,6 +782,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
     g.BH = BH;
     g.n_items = BH * nt;
     g.kv_len = a.kv_len;
+    g.mask = a.block_mask;
     e = launch_pdl(kern, dim3(min(g.n_items, sm_count())), dim3(kThreads), L::kSmem, stream,
                    a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g,
                    Npad, a.scale, a.status, a.wait_limit);

@@ -150,6 +150,22 @@ int fa_blocksparse_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int H, int N, int d, float scale, const uint8_t* block_mask, int block_size,
                        struct CUstream_st* stream);
 
+/* Backward pass of the block-sparse forward (fa_blocksparse_fwd): dQ, dK, dV
+ * of L = sum(dO * O) when attention is restricted to the kept 128 x 128
+ * blocks. Masked blocks contribute nothing, so the recomputation and the five
+ * products run only over kept blocks (condensed paper sample_paper.md,
+ * section 4: block-sparse FlashAttention, IO proportional to the sparsity).
+ *   q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes : as fa_bwd
+ *                 (o and lse from fa_blocksparse_fwd with the same mask and scale);
+ *   block_mask  : as fa_blocksparse_fwd (DEVICE uint8 [nb][nb], nonzero = kept);
+ *   block_size  : must be 128 (else FA_ERR_UNSUPPORTED).
+ * Key tiles kept by no query tile get dK = dV = 0; query rows of a tile that
+ * keeps no key tile get dQ = 0. Errors as fa_bwd. */
+int fa_blocksparse_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H, int N, int d, float scale, const uint8_t* block_mask, int block_size,
+                       void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
 /* Device-side status of the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT
  * if a bounded wait inside a kernel gave up since the last call. Reading
  * clears it. Call only after synchronising the streams that ran the

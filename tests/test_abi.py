@@ -31,7 +31,7 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     names = declared_symbols()
     for n in ("fa_fwd", "fa_fwd_kpad", "fa_bwd", "fa_bwd_workspace_bytes", "fa_blocksparse_fwd",
-              "fa_device_status", "fa_status_string", "fa_selftest_wait_timeout"):
+              "fa_blocksparse_bwd", "fa_device_status", "fa_status_string", "fa_selftest_wait_timeout"):
         assert n in names
 
 

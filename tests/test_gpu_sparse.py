@@ -1,12 +1,12 @@
-"""Block-sparse forward parity: the CUDA path vs the dense oracle with the
-masked 128 x 128 blocks set to -inf."""
+"""Block-sparse forward and backward parity: the CUDA path vs the dense oracle
+with the masked 128 x 128 blocks set to -inf."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads as W
-from _util import check_fwd, cuda, f64
+from _util import check_fwd, check_grads, cuda, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -57,3 +57,59 @@ def test_sparse_full_size_workload(fa):
     rows = np.concatenate([np.arange(b * 128, (b + 1) * 128) for b in blocks])
     o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, block_mask=m, rows=rows)
     check_fwd(f64(o)[:, :, rows], f64(lse)[:, :, rows], o_ref, l_ref, "blocksparse full size")
+
+
+# ---------------------------------------------------------------- backward
+def _sparse_bwd(fa, x, mask, scale):
+    q, k, v, do = cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["dout"])
+    m = torch.from_numpy(mask).cuda()
+    o, lse = fa.blocksparse_forward(q, k, v, m, scale=scale)
+    g = fa.blocksparse_backward(q, k, v, o, do, lse, m, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    return g
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [512, 1000])
+def test_sparse_bwd_small_random_masks(fa, d, N):
+    w = W.Workload("generic", 2, 2, N, d, causal=False, backward=True)
+    x = W.make_inputs(w, 31)
+    nb = (N + 127) // 128
+    g = np.random.default_rng(N + d + 1)
+    mask = (g.random((nb, nb)) < 0.5).astype(np.uint8)
+    mask[0, :] = 1
+    mask[1, :] = 0            # a query block that sees nothing: its dQ rows are 0
+    mask[:, 2] = 0            # a key block no query block keeps: its dK, dV rows are 0
+    grads = _sparse_bwd(fa, x, mask, w.scale)
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, block_mask=mask)
+    check_grads(grads, ref, f"sparse bwd d={d} N={N}")
+    dq, dk, dv = (f64(t) for t in grads)
+    assert np.all(dq[:, :, 128:256] == 0)
+    assert np.all(dk[:, :, 256:384] == 0) and np.all(dv[:, :, 256:384] == 0)
+
+
+def test_sparse_bwd_all_ones_equals_dense(fa):
+    w = W.Workload("generic", 1, 3, 640, 64, causal=False, backward=True)
+    x = W.make_inputs(w, 32)
+    ones = np.ones((5, 5), dtype=np.uint8)
+    gs = _sparse_bwd(fa, x, ones, w.scale)
+    q, k, v, do = cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["dout"])
+    o, lse = fa.forward(q, k, v)
+    gd = fa.backward(q, k, v, o, do, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(gs[1], gd[1]) and torch.equal(gs[2], gd[2])
+    # dQ sums tiles with fp32 reduce-adds: equal up to reduction order
+    assert torch.allclose(gs[0].float(), gd[0].float(), rtol=0, atol=1e-2)
+
+
+def test_sparse_bwd_full_size_workload(fa):
+    w = W.WORKLOADS["blocksparse"]
+    x = W.make_inputs(w, 0)
+    mask = x["block_mask"].numpy()
+    grads = _sparse_bwd(fa, x, mask, w.scale)
+    heads = [(1, 3)]
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, block_mask=mask,
+                          heads=heads)
+    for b, h in heads:
+        check_grads([f64(t)[b, h] for t in grads], [r[b, h] for r in ref], f"blocksparse bwd {(b, h)}")

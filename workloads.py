@@ -67,8 +67,8 @@ WORKLOADS = {
     # BERT-large shaped attention: 16 heads of 64, sequence 512, key padding.
     "bert_large": Workload("bert_large", 16, 16, 512, 64, causal=False, backward=True,
                            kv_len_range=(256, 512)),
-    # Block-sparse forward at sequence 16K.
-    "blocksparse": Workload("blocksparse", 2, 8, 16384, 64, causal=False, backward=False,
+    # Block-sparse forward and backward at sequence 16K.
+    "blocksparse": Workload("blocksparse", 2, 8, 16384, 64, causal=False, backward=True,
                             sparse=True),
 }
 for _n in (4096, 8192, 16384):
