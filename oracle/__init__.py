@@ -5,6 +5,8 @@ product path never imports it.
 """
 from .attention import (BLOCK, backward, forward, head_backward, head_backward_jacobian,
                         head_forward, head_probs, loss, to_f64, visible)
+from .dropout import draw_bytes, keep_mask, multiplier, philox4x32_10, rescale, threshold
 
 __all__ = ["BLOCK", "backward", "forward", "head_backward", "head_backward_jacobian",
-           "head_forward", "head_probs", "loss", "to_f64", "visible"]
+           "head_forward", "head_probs", "loss", "to_f64", "visible", "draw_bytes", "keep_mask",
+           "multiplier", "philox4x32_10", "rescale", "threshold"]

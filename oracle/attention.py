@@ -35,7 +35,8 @@ Readings taken where the pages are silent (all stated in the design notes):
 the stored per-row statistic is the natural-log logsumexp including the scale;
 causal keeps j <= i (square); key padding masks keys j >= kv_len[b] for every
 query row; a block mask (block size 128) masks whole 128 x 128 blocks; a row
-with no visible key gives O = 0, LSE = -inf and zero gradients.
+with no visible key gives O = 0, LSE = -inf and zero gradients. Dropout, when
+asked for, follows oracle/dropout.py (inverted dropout on P, Philox draws).
 
 Pins: every function here is checked in tests/test_oracle.py against closed
 forms, invariants, special cases, a hand-derived worked example
@@ -94,9 +95,14 @@ def _probs(q_rows, k, scale, keep):
     return p, lse
 
 
-def head_forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, rows=None):
+def head_forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, rows=None,
+                 drop=None):
     """One head. q [Nq,d], k [Nk,d], v [Nk,dv] fp64. Returns O [r,dv], LSE [r]
-    for the requested query rows (all rows by default)."""
+    for the requested query rows (all rows by default).
+
+    ``drop``: optional function (rows, n_k) -> [len(rows), n_k] multiplier
+    Z / (1 - p') (oracle.dropout.multiplier); then O = (P * drop) V while LSE
+    stays that of the undropped scores."""
     q, k, v = to_f64(q), to_f64(k), to_f64(v)
     rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows)
     o = np.empty((len(rows), v.shape[1]))
@@ -105,6 +111,8 @@ def head_forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, row
     for rr in _chunks(rows, k.shape[0]):
         keep = visible(rr, k.shape[0], causal, kv_len, block_mask)
         p, l = _probs(q[rr], k, scale, keep)
+        if drop is not None:
+            p = p * drop(rr, k.shape[0])
         o[pos:pos + len(rr)] = p @ v
         lse[pos:pos + len(rr)] = l
         pos += len(rr)
@@ -118,8 +126,12 @@ def head_probs(q, k, scale, causal=False, kv_len=None, block_mask=None):
     return _probs(q, k, scale, keep)[0]
 
 
-def head_backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None):
-    """One head's gradients of L = sum(dO * O): returns dQ, dK, dV (fp64)."""
+def head_backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None, drop=None):
+    """One head's gradients of L = sum(dO * O): returns dQ, dK, dV (fp64).
+
+    With ``drop`` (as in head_forward) O = Pd V with Pd = P * drop, so
+    dV = Pd^T dO and the gradient reaching P is dP = (dO V^T) * drop; the
+    softmax Jacobian is then applied to that dP exactly as without dropout."""
     q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
@@ -128,21 +140,28 @@ def head_backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=No
         keep = visible(rr, k.shape[0], causal, kv_len, block_mask)
         p, _ = _probs(q[rr], k, scale, keep)
         dp = dout[rr] @ v.T
+        pd = p
+        if drop is not None:
+            mult = drop(rr, k.shape[0])
+            dp = dp * mult
+            pd = p * mult
         rowdot = (p * dp).sum(axis=1)
         ds = p * (dp - rowdot[:, None])
-        dv += p.T @ dout[rr]
+        dv += pd.T @ dout[rr]
         dk += scale * (ds.T @ q[rr])
         dq[rr] = scale * (ds @ k)
     return dq, dk, dv
 
 
-def head_backward_jacobian(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None):
+def head_backward_jacobian(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None,
+                           drop=None):
     """Same gradients, with each row's softmax Jacobian built as a matrix.
     Quadratic memory per row: tiny inputs only."""
     q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
     p = head_probs(q, k, scale, causal, kv_len, block_mask)
-    dv = p.T @ dout
-    dp = dout @ v.T
+    mult = np.ones_like(p) if drop is None else drop(np.arange(p.shape[0]), p.shape[1])
+    dv = (p * mult).T @ dout
+    dp = (dout @ v.T) * mult
     ds = np.empty_like(p)
     for i in range(p.shape[0]):
         jac = np.diag(p[i]) - np.outer(p[i], p[i])
@@ -154,10 +173,21 @@ def _kvl(kv_len, b):
     return None if kv_len is None else int(np.asarray(kv_len).reshape(-1)[b])
 
 
-def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, heads=None, rows=None):
+def _drop(dropout, bh):
+    if dropout is None:
+        return None
+    from .dropout import multiplier
+    p, seed, offset = dropout
+    return multiplier(bh, seed, offset, p)
+
+
+def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, heads=None, rows=None,
+            dropout=None):
     """Batched forward over [B,H,N,d]. Returns O [B,H,r,d], LSE [B,H,r].
     ``heads``: optional list of (b, h) to compute (others left NaN).
-    ``rows``: optional query-row subset (same for every head)."""
+    ``rows``: optional query-row subset (same for every head).
+    ``dropout``: optional (p, seed, offset); head (b, h) uses the keep mask of
+    problem b*H + h (oracle.dropout)."""
     q, k, v = to_f64(q), to_f64(k), to_f64(v)
     B, H, N, _ = q.shape
     nr = N if rows is None else len(rows)
@@ -166,12 +196,15 @@ def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, heads=No
     todo = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for b, h in todo:
         o[b, h], lse[b, h] = head_forward(q[b, h], k[b, h], v[b, h], scale, causal,
-                                          _kvl(kv_len, b), block_mask, rows)
+                                          _kvl(kv_len, b), block_mask, rows,
+                                          _drop(dropout, b * H + h))
     return o, lse
 
 
-def backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None, heads=None):
-    """Batched backward over [B,H,N,d]. Returns dQ, dK, dV (NaN outside ``heads``)."""
+def backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None, heads=None,
+             dropout=None):
+    """Batched backward over [B,H,N,d]. Returns dQ, dK, dV (NaN outside ``heads``).
+    ``dropout``: as in forward."""
     q, k, v, dout = to_f64(q), to_f64(k), to_f64(v), to_f64(dout)
     B, H = q.shape[:2]
     dq = np.full(q.shape, np.nan)
@@ -180,11 +213,12 @@ def backward(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None, h
     todo = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
     for b, h in todo:
         dq[b, h], dk[b, h], dv[b, h] = head_backward(q[b, h], k[b, h], v[b, h], dout[b, h],
-                                                     scale, causal, _kvl(kv_len, b), block_mask)
+                                                     scale, causal, _kvl(kv_len, b), block_mask,
+                                                     _drop(dropout, b * H + h))
     return dq, dk, dv
 
 
-def loss(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None):
+def loss(q, k, v, dout, scale, causal=False, kv_len=None, block_mask=None, drop=None):
     """L = sum(dO * O) for one head (the function the backward differentiates)."""
-    o, _ = head_forward(q, k, v, scale, causal, kv_len, block_mask)
+    o, _ = head_forward(q, k, v, scale, causal, kv_len, block_mask, drop=drop)
     return float((to_f64(dout) * o).sum())
