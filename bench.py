@@ -52,30 +52,31 @@ def peaks():
 
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by kernel and
 # workload, valid only while the kernel's sources are unchanged (first 16 hex
-# digits of the SHA-256 of its .cu file followed by the shared PTX header when
-# it was captured; see profiles/).
-NCU_TRAFFIC = {
-    ("bwd_main", "gpt2_small"): (80_988_416, "fa_bwd.cu", "65bc2805d8b2193f"),
-    ("fwd", "gpt2_small"): (37_845_504, "fa_fwd.cu", "4d6d1983950bf061"),
-}
+# digits of the SHA-256 of the kernel's source followed by the shared device
+# headers when it was captured; see profiles/).
+NCU_TRAFFIC = {}
+_SHARED_HEADERS = ("fa_ptx.cuh", "fa_philox.cuh")
 
 
-def ncu_traffic(kernel: str, workload: str):
+def source_digest(src: str):
     import hashlib
-    entry = NCU_TRAFFIC.get((kernel, workload))
-    if entry is None:
-        return None
-    nbytes, src, digest = entry
     csrc = os.path.join(ROOT, "exact_io_aware_11_gb300", "csrc")
     h = hashlib.sha256()
     try:
-        for name in (src, "fa_ptx.cuh"):
+        for name in (src, *_SHARED_HEADERS):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(f.read())
     except OSError:
         return None
-    now = h.hexdigest()[:16]
-    return nbytes if now == digest else None
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    entry = NCU_TRAFFIC.get((kernel, workload))
+    if entry is None:
+        return None
+    nbytes, src, digest = entry
+    return nbytes if source_digest(src) == digest else None
 
 
 def flops(w: W.Workload, kv_len=None):
@@ -165,10 +166,17 @@ class Step:
         self.ws_bytes = fa.bwd_workspace_bytes(B, H, N, d)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.L = fa.lib()
+        self.offset = 0  # dropout counter offset, advanced once per step
 
     def fwd(self, stream):
         w, L = self.w, self.L
-        if self.mask is not None:
+        if w.dropout > 0:
+            rc = L.fa_dropout_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                  self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
+                                  int(w.causal), w.scale,
+                                  None if self.kv is None else self.kv.data_ptr(), w.dropout,
+                                  w.dropout_seed, self.offset, stream)
+        elif self.mask is not None:
             rc = L.fa_blocksparse_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
                                       self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
                                       w.scale, self.mask.data_ptr(), 128, stream)
@@ -181,6 +189,18 @@ class Step:
 
     def bwd_stages(self, stream):
         w, L = self.w, self.L
+        if w.dropout > 0:  # one call runs all three kernels
+            yield L.fa_dropout_bwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                   self.o.data_ptr(), self.do.data_ptr(), self.lse.data_ptr(),
+                                   self.dq.data_ptr(), self.dk.data_ptr(), self.dv.data_ptr(),
+                                   w.B, w.H, w.N, w.d, int(w.causal), w.scale,
+                                   None if self.kv is None else self.kv.data_ptr(), w.dropout,
+                                   w.dropout_seed, self.offset, self.ws.data_ptr(), self.ws_bytes,
+                                   stream)
+            self.offset += 1  # the next step draws a fresh mask
+            yield 0
+            yield 0
+            return
         if self.mask is not None:  # block-sparse: one call runs all three kernels
             yield L.fa_blocksparse_bwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
                                        self.o.data_ptr(), self.do.data_ptr(), self.lse.data_ptr(),
@@ -455,6 +475,8 @@ def sweep(fa, dev, flush, pk):
             r["bwd_pct_peak"] = round(r["bwd_tflops"] / pk["bf16_tflops"], 4)
             if w.sparse:
                 r["bwd_timing"] = "one fa_blocksparse_bwd call (preprocess, main, dQ convert)"
+            elif w.dropout > 0:
+                r["bwd_timing"] = "one fa_dropout_bwd call (preprocess, main, dQ convert)"
             else:
                 r["bwd_main_ms"] = round(statistics.median(t["bwd_main"]), 4)
         res[name] = r

@@ -21,6 +21,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_DEVICE_TIMEOU
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
+_U64 = ctypes.c_uint64
+_U32 = ctypes.c_uint32
 
 SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
@@ -35,6 +37,10 @@ SIGNATURES = {
     "fa_blocksparse_bwd": (_I, [_P] * 9 + [_I, _I, _I, _I, _F, _P, _I, _P, ctypes.c_size_t, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P]),
     "fa_blocksparse_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _P, _I, _P]),
+    "fa_dropout_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _F, _U64, _U32, _P]),
+    "fa_dropout_bwd": (_I, [_P] * 9 + [_I, _I, _I, _I, _I, _F, _P, _F, _U64, _U32, _P,
+                                       ctypes.c_size_t, _P]),
+    "fa_dropout_mask": (_I, [_I, _I, _I, _F, _U64, _U32, _P, _P]),
     "fa_device_status": (_I, []),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_longlong, _P]),
@@ -180,6 +186,71 @@ def blocksparse_backward(q, k, v, o, dout, lse, block_mask, scale: float | None 
                                   int(block_size), ws.data_ptr(), ws.numel(), _stream_ptr(stream))
     _raise(rc, "fa_blocksparse_bwd")
     return dq, dk, dv
+
+
+def _check_dropout(p, seed, offset):
+    p = float(p)
+    if not (0.0 <= p < 1.0):
+        raise ValueError("dropout_p must be in [0, 1)")
+    if not (0 <= int(seed) < 2 ** 64) or not (0 <= int(offset) < 2 ** 32):
+        raise ValueError("seed must fit in 64 bits and offset in 32 bits")
+    return p, int(seed), int(offset)
+
+
+def dropout_forward(q, k, v, dropout_p: float, seed: int, offset: int = 0, causal: bool = False,
+                    scale: float | None = None, kv_len=None, out=None, lse=None, stream=None):
+    """O, LSE of attention with fused dropout on P (fa_dropout_fwd)."""
+    _check_qkv(q, k, v)
+    p, seed, offset = _check_dropout(dropout_p, seed, offset)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if kv_len is not None and (kv_len.dtype != torch.int32 or not kv_len.is_cuda):
+        raise ValueError("kv_len must be a CUDA int32 tensor of shape [B]")
+    rc = lib().fa_dropout_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              l.data_ptr(), B, H, N, d, int(bool(causal)), scale, _ptr(kv_len), p,
+                              seed, offset, _stream_ptr(stream))
+    _raise(rc, "fa_dropout_fwd")
+    return o, l
+
+
+def dropout_backward(q, k, v, o, dout, lse, dropout_p: float, seed: int, offset: int = 0,
+                     causal: bool = False, scale: float | None = None, kv_len=None,
+                     workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of dropout_forward with the same dropout_p, seed and offset
+    (fa_dropout_bwd)."""
+    _check_qkv(q, k, v, o, dout)
+    p, seed, offset = _check_dropout(dropout_p, seed, offset)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    need = bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if kv_len is not None and (kv_len.dtype != torch.int32 or not kv_len.is_cuda):
+        raise ValueError("kv_len must be a CUDA int32 tensor of shape [B]")
+    rc = lib().fa_dropout_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, d, int(bool(causal)), scale, _ptr(kv_len),
+                              p, seed, offset, ws.data_ptr(), ws.numel(), _stream_ptr(stream))
+    _raise(rc, "fa_dropout_bwd")
+    return dq, dk, dv
+
+
+def dropout_mask(B: int, H: int, N: int, dropout_p: float, seed: int, offset: int = 0,
+                 device=None, out=None, stream=None):
+    """uint8 [B, H, N, N] keep decisions (1 = kept) of the dropout calls with the
+    same arguments (fa_dropout_mask)."""
+    p, seed, offset = _check_dropout(dropout_p, seed, offset)
+    keep = (torch.empty((B, H, N, N), dtype=torch.uint8, device=device or "cuda")
+            if out is None else out)
+    if not keep.is_cuda or keep.dtype != torch.uint8 or not keep.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA uint8 tensor [B, H, N, N]")
+    rc = lib().fa_dropout_mask(B, H, N, p, seed, offset, keep.data_ptr(), _stream_ptr(stream))
+    _raise(rc, "fa_dropout_mask")
+    return keep
 
 
 def device_status() -> int:

@@ -118,13 +118,30 @@ int check_common(int B, int H, int N, int d, float scale) {
   return FA_OK;
 }
 
+// Dropout parameters from the caller's probability, seed and offset: the drop
+// threshold t = round(256 p) (at most 255) on one random byte per element,
+// kept entries scaled by 256 / (256 - t). Returns false for p outside [0, 1).
+bool make_dropout(float p, uint64_t seed, uint32_t offset, DropoutParams* out) {
+  if (!std::isfinite(p) || p < 0.f || p >= 1.f) return false;
+  int t = static_cast<int>(std::floor(256.0 * static_cast<double>(p) + 0.5));
+  if (t > 255) t = 255;
+  out->k0 = static_cast<uint32_t>(seed & 0xffffffffu);
+  out->k1 = static_cast<uint32_t>(seed >> 32);
+  out->offset = offset;
+  out->thresh4 = static_cast<uint32_t>(t) * 0x01010101u;
+  out->rescale = static_cast<float>(256.0 / (256.0 - t));
+  out->enabled = 1;
+  return true;
+}
+
 size_t tensor_bytes(int B, int H, int N, int d, size_t elem) {
   return static_cast<size_t>(B) * H * N * d * elem;
 }
 
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int N, int d, int causal, float scale, const int32_t* kv_len,
-               const uint8_t* block_mask, cudaStream_t stream) {
+               const uint8_t* block_mask, cudaStream_t stream,
+               const DropoutParams* drop = nullptr) {
   int st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
@@ -155,6 +172,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   a.scale = scale;
   a.kv_len = kv_len;
   a.block_mask = block_mask;
+  if (drop) a.drop = *drop;
   a.status = dev.status;
   a.wait_limit = kWaitLimitCycles;
   return launch_fwd(a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -177,7 +195,7 @@ struct BwdPtrs {
 // not use may be NULL; every pointer a stage uses must be non-NULL.
 int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int causal, float scale,
                const int32_t* kv_len, size_t workspace_bytes, cudaStream_t stream,
-               const uint8_t* block_mask = nullptr) {
+               const uint8_t* block_mask = nullptr, const DropoutParams* drop = nullptr) {
   int st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
   const bool pre = stages & kBwdStagePre, mainst = stages & kBwdStageMain,
@@ -235,6 +253,7 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
   a.scale = scale;
   a.kv_len = kv_len;
   a.block_mask = block_mask;
+  if (drop) a.drop = *drop;
   a.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
   a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   a.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
@@ -316,6 +335,38 @@ int fa_blocksparse_bwd(const void* q, const void* k, const void* v, const void* 
   const BwdPtrs p{q, k, v, o, dout, lse, dq, dk, dv, workspace};
   return bwd_common(kBwdStageAll, p, B, H, N, d, 0, scale, nullptr, workspace_bytes, stream,
                     block_mask);
+}
+
+int fa_dropout_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int N, int d, int causal, float scale, const int32_t* kv_len,
+                   float dropout_p, uint64_t seed, uint32_t offset, struct CUstream_st* stream) {
+  DropoutParams drop{};
+  if (!make_dropout(dropout_p, seed, offset, &drop)) return FA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, H, N, d, causal, scale, kv_len, nullptr, stream, &drop);
+}
+
+int fa_dropout_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, const int32_t* kv_len, float dropout_p, uint64_t seed,
+                   uint32_t offset, void* workspace, size_t workspace_bytes,
+                   struct CUstream_st* stream) {
+  DropoutParams drop{};
+  if (!make_dropout(dropout_p, seed, offset, &drop)) return FA_ERR_INVALID_ARG;
+  const BwdPtrs p{q, k, v, o, dout, lse, dq, dk, dv, workspace};
+  return bwd_common(kBwdStageAll, p, B, H, N, d, causal, scale, kv_len, workspace_bytes, stream,
+                    nullptr, &drop);
+}
+
+int fa_dropout_mask(int B, int H, int N, float dropout_p, uint64_t seed, uint32_t offset,
+                    uint8_t* keep, struct CUstream_st* stream) {
+  DropoutParams drop{};
+  if (!make_dropout(dropout_p, seed, offset, &drop)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || !keep) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  const int st = current_device_info(&dev);
+  if (st != FA_OK) return st;
+  return launch_dropout_mask(drop, B * H, N, keep, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N,

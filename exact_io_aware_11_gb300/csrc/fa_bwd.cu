@@ -1,741 +1,11 @@
-// Backward pass of exact attention as three sm_103a kernels.
-//
-// Method: the attention matrix is not read back from HBM; it is recomputed on
-// chip, tile by tile, from Q, K and the per-row statistic saved by the forward
-// pass (condensed paper sample_paper.md, section 3, "in the backward pass, the
-// attention matrix is recomputed on-chip from stored statistics"; section 5,
-// "tiling and recomputation"). With LSE the natural-log logsumexp:
-//   P = exp(scale * Q K^T - LSE),   dV = P^T dO,   dP = dO V^T,
-//   D = rowsum(dO * O) (= rowsum(P * dP)),   dS = P * (dP - D),
-//   dQ = scale * dS K,   dK = scale * dS^T Q.
-//
-// 1. bwd_pre_kernel   D = rowsum(dO * O), LSE * log2(e), zero the fp32 dQ
-//                     accumulator (bandwidth-bound, 16-byte accesses).
-// 2. bwd_main_kernel  persistent, one CTA per SM; a work item is one 128-key
-//                     tile j of one (batch, head). K_j and V_j stay in shared
-//                     memory, dK_j and dV_j accumulate in TMEM, and the CTA
-//                     loops over the Q tiles i:
-//                       S^T  = K_j Q_i^T    TMEM, key rows on lanes
-//                       dP^T = V_j dO_i^T   TMEM
-//                       P^T  = exp2(S^T * scale*log2e - LSE2_i), bf16, written
-//                              back into the S^T columns and used from TMEM
-//                       dV_j += P^T dO_i
-//                       dS^T = P^T * (dP^T - D_i), bf16 -> shared memory
-//                       dK_j += dS^T Q_i
-//                       dQ_i  = dS K_j      TMEM -> shared memory (fp32) -> one
-//                              TMA bulk reduce-add per 32-column chunk into the
-//                              fp32 workspace accumulator
-//                     Warps 0-7 compute P and dS (warps w and w+4 share the
-//                     key rows of TMEM lane quarter w % 4 and split the 128
-//                     query columns), warp 8 issues TMA, warp 9 issues
-//                     tcgen05.mma, warps 10-13 drain dQ and, at the end of
-//                     an item, write dK_j / dV_j from TMEM. S^T of tile i+1
-//                     (also of the next item's first tile) is computed while
-//                     dS of tile i is being formed.
-// 3. dq_convert_kernel  dQ bf16 = fp32 accumulator.
-#include <cuda_bf16.h>
-
-#include "fa_internal.h"
-#include "fa_ptx.cuh"
+// Backward pass of exact attention: the preprocess and dQ-conversion stages,
+// the dense, causal, key-padded and block-sparse variants of the main kernel
+// (fa_bwd_kernel.cuh; the dropout variants are compiled in fa_bwd_dropout.cu)
+// and the watchdog self-test kernel.
+#include "fa_bwd_kernel.cuh"
 
 namespace fa {
 namespace {
-
-constexpr int kThreads = 448;
-constexpr int kChunk = 128 * 128;  // one 128-row x 128-byte swizzled chunk
-constexpr float kLog2e = 1.4426950408889634f;
-
-template <int D>
-struct BwdLayout {
-  static constexpr int kChunks = D / 64;
-  static constexpr int kTile = kChunks * kChunk;     // 128 x D bf16
-  static constexpr int kKVS = (D == 64) ? 2 : 1;     // K/V stages (next item's K/V prefetched)
-  static constexpr int kQS = 2;                      // Q (+ LSE2 / D) stages
-  static constexpr int kDS = (D == 64) ? 2 : 1;      // dO stages
-  static constexpr int kDQChunks = (D == 64) ? 2 : 1;  // 128 x 32 fp32 chunks staged at once
-  static constexpr int kKV = 0;                      // stage s: K at kKV + 2 s kTile, then V
-  static constexpr int kQ = kKV + 2 * kKVS * kTile;
-  static constexpr int kDO = kQ + kQS * kTile;
-  static constexpr int kStat = kDO + kDS * kTile;    // per Q stage: lse2[128], delta[128]
-  static constexpr int kDSb = kStat + kQS * 1024;    // dS^T, bf16, 2 chunks
-  static constexpr int kDQ = kDSb + 2 * kChunk;      // dQ staging (fp32, 128-byte swizzle)
-  static constexpr int kBar = kDQ + kDQChunks * kChunk;
-  static constexpr int kEnd = kBar + 256;
-  static constexpr int kSmem = kEnd + 1024;
-  // TMEM columns
-  static constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256, kTDK = 256 + D;
-  static constexpr uint32_t kTDQ = (D == 64) ? 384 : 128;  // d=128: dQ reuses the dP^T columns
-};
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  const uint32_t a = smem_u32(p);
-  return p + ((1024u - (a & 1023u)) & 1023u);
-}
-
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
-                                                  int y, int z) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
-                                             int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// ----------------------------------------------------------------- preprocess
-template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
-                                                      const __nv_bfloat16* __restrict__ dout,
-                                                      const float* __restrict__ lse,
-                                                      float* __restrict__ lse2,
-                                                      float* __restrict__ delta,
-                                                      float* __restrict__ dq_acc, int BH, int N,
-                                                      int Npad) {
-  constexpr int kPer = D / 8;  // threads per row (8 elements = 16 bytes each)
-  grid_dep_wait();
-  grid_dep_launch();
-  const long long total = static_cast<long long>(BH) * Npad * kPer;
-  const long long total32 = (total + 31) & ~31LL;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total32;
-       g += stride) {
-    const bool in = g < total;
-    const long long row = g / kPer;  // over [BH, Npad]
-    const int part = static_cast<int>(g % kPer);
-    const int bh = static_cast<int>(row / Npad);
-    const int n = static_cast<int>(row % Npad);
-    const bool valid = in && n < N;
-    float acc = 0.f;
-    if (valid) {
-      const size_t off = (static_cast<size_t>(bh) * N + n) * D + part * 8;
-      const uint4 a = *reinterpret_cast<const uint4*>(o + off);
-      const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 x = __bfloat1622float2(a2[i]);
-        const float2 y = __bfloat1622float2(b2[i]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-      }
-    }
-#pragma unroll
-    for (int w = 1; w < kPer; w <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
-    if (in) {
-      float4* z = reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * D + part * 8);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (part == 0) {
-        delta[row] = valid ? acc : 0.f;
-        float l2 = INFINITY;  // padding rows and rows that saw no key get P = 0
-        if (valid) {
-          const float v = lse[static_cast<size_t>(bh) * N + n];
-          if (v != -INFINITY) l2 = v * kLog2e;
-        }
-        lse2[row] = l2;
-      }
-    }
-  }
-}
-
-// ----------------------------------------------------------------- dQ convert
-template <int D>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ dq_acc,
-                                                         __nv_bfloat16* __restrict__ dq, int BH,
-                                                         int N, int Npad) {
-  constexpr int kPer = D / 8;
-  grid_dep_wait();
-  grid_dep_launch();
-  const long long total = static_cast<long long>(BH) * N * kPer;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
-       g += stride) {
-    const long long row = g / kPer;  // over [BH, N]
-    const int part = static_cast<int>(g % kPer);
-    const long long bh = row / N;
-    const long long n = row % N;
-    const float4* src = reinterpret_cast<const float4*>(dq_acc + (bh * Npad + n) * D + part * 8);
-    const float4 a = src[0], b = src[1];
-    uint4 w;
-    w.x = pack_bf16(a.x, a.y);
-    w.y = pack_bf16(a.z, a.w);
-    w.z = pack_bf16(b.x, b.y);
-    w.w = pack_bf16(b.z, b.w);
-    *reinterpret_cast<uint4*>(dq + row * D + part * 8) = w;
-  }
-}
-
-// ----------------------------------------------------------------- work items
-// One work item: key tile j of one (batch, head), met by Q tiles i0 .. nt-1.
-// An item whose keys all lie beyond the valid length has no iterations; its
-// dK and dV rows are written as zeros.
-struct BwdGrid {
-  int H, N, nt, BH, n_items;
-  const int32_t* kv_len;
-  const uint8_t* mask;  // block-sparse: uint8 [nt][nt], nonzero = (query tile, key tile) kept
-};
-
-struct BwdItem {
-  int bh, j, i0, n_iter, kv_bound;  // i0: first query tile met (the rest follow bwd_next_row)
-};
-
-template <bool SPARSE>
-__device__ __forceinline__ int bwd_next_row(const BwdGrid& g, int j, int i);
-
-// Item k. Causal items are ordered heaviest first (key tile j meets nt - j
-// query tiles); otherwise a head's key tiles are consecutive, so that CTAs
-// running at the same time stream the same Q and dO tiles through L2.
-template <bool CAUSAL, bool SPARSE = false>
-__device__ __forceinline__ BwdItem make_bwd_item(const BwdGrid& g, int k) {
-  BwdItem x;
-  if (CAUSAL) {
-    x.j = k / g.BH;
-    x.bh = k - x.j * g.BH;
-  } else {
-    x.bh = k / g.nt;
-    x.j = k - x.bh * g.nt;
-  }
-  x.kv_bound = g.N;
-  if (g.kv_len != nullptr) x.kv_bound = min(g.N, max(0, g.kv_len[x.bh / g.H]));
-  x.i0 = CAUSAL ? x.j : 0;
-  x.n_iter = x.j * kBlock < x.kv_bound ? g.nt - x.i0 : 0;
-  if constexpr (SPARSE) {  // the query tiles whose mask row keeps key tile j
-    int n = 0;
-    for (int i = 0; i < g.nt; ++i) n += g.mask[static_cast<size_t>(i) * g.nt + x.j] != 0;
-    x.n_iter = n;
-    x.i0 = bwd_next_row<true>(g, x.j, 0);
-  }
-  return x;
-}
-
-// The first query tile >= i that meets key tile j: i itself unless a block
-// mask says otherwise (nt if there is none).
-template <bool SPARSE>
-__device__ __forceinline__ int bwd_next_row(const BwdGrid& g, int j, int i) {
-  if constexpr (SPARSE) {
-    while (i < g.nt && g.mask[static_cast<size_t>(i) * g.nt + j] == 0) ++i;
-  }
-  return i;
-}
-
-// The r-th item of this CTA: a snake over the item list; -1 when there is none.
-__device__ __forceinline__ int bwd_item_of(const BwdGrid& g, int r) {
-  const int G = gridDim.x, c = blockIdx.x;
-  if (r * G >= g.n_items) return -1;
-  const int k = r * G + ((r & 1) ? G - 1 - c : c);
-  return k < g.n_items ? k : -1;
-}
-
-// Position of the MMA issuer in this CTA's flattened sequence of iterations:
-// iteration `it` of `n` of the t-th item that has iterations, the g-th
-// iteration overall (ring slots and barrier phases follow t and g).
-template <bool CAUSAL, bool SPARSE>
-struct BwdCursor {
-  int r = 0, it = 0, n = 0, t = 0, g = 0;
-  bool valid = false;
-  __device__ void seek(const BwdGrid& G) {
-    for (;; ++r) {
-      const int k = bwd_item_of(G, r);
-      if (k < 0) {
-        valid = false;
-        return;
-      }
-      const int n_iter = make_bwd_item<CAUSAL, SPARSE>(G, k).n_iter;
-      if (n_iter > 0) {
-        n = n_iter;
-        it = 0;
-        valid = true;
-        return;
-      }
-    }
-  }
-  __device__ void next(const BwdGrid& G) {
-    ++g;
-    if (++it < n) return;
-    ++t;
-    ++r;
-    seek(G);
-  }
-};
-
-// ----------------------------------------------------------------- main kernel
-// Persistent: one CTA per SM walks its items; barrier phases run on across
-// items, K/V of the next item are prefetched when shared memory holds two
-// stages (d = 64), and dK/dV are written from TMEM by the dQ drain warps while
-// the compute warps already form P of the next item.
-template <int D, bool CAUSAL, bool SPARSE>
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dqacc, __nv_bfloat16* __restrict__ dk,
-                    __nv_bfloat16* __restrict__ dv, const float* __restrict__ lse2,
-                    const float* __restrict__ delta, BwdGrid grid, int Npad, float scale,
-                    int* status, long long wait_limit) {
-  using L = BwdLayout<D>;
-  constexpr int QS = L::kQS, DS = L::kDS, KVS = L::kKVS;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* bar_kvfull = bars + 0;    // [KVS]
-  uint64_t* bar_kvempty = bars + 2;   // [KVS]
-  uint64_t* bar_qfull = bars + 4;     // [QS]
-  uint64_t* bar_qempty = bars + 6;    // [QS]
-  uint64_t* bar_dofull = bars + 8;    // [DS]
-  uint64_t* bar_doempty = bars + 10;  // [DS]
-  uint64_t* bar_sfull = bars + 12;
-  uint64_t* bar_dpfull = bars + 13;
-  uint64_t* bar_pready = bars + 14;
-  uint64_t* bar_dsready = bars + 15;
-  uint64_t* bar_dsfree = bars + 16;
-  uint64_t* bar_dqfull = bars + 17;
-  uint64_t* bar_dqfree = bars + 18;
-  uint64_t* bar_accfull = bars + 19;  // dV and dK of an item complete
-  uint64_t* bar_dvempty = bars + 20;  // dV read out of TMEM
-  uint64_t* bar_dkempty = bars + 21;  // dK read out of TMEM
-  uint64_t* bar_final = bars + 22;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
-  int* abort_flag = reinterpret_cast<int*>(bars + 24);
-  uint64_t* bar_dpfree = bars + 25;   // dP^T read out of TMEM (d = 64)
-  // d = 64: dQ has TMEM columns of its own, so dP^T of the next Q tile can be
-  // issued as soon as the compute warps have read dP^T of this one, ahead of
-  // this tile's dK and dQ MMAs in the in-order tensor pipe.
-  constexpr bool kEarlyDP = (D == 64);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int N = grid.N;
-  const float scale_log2 = scale * kLog2e;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < KVS; ++s) {
-      mbar_init(bar_kvfull + s, 1);
-      mbar_init(bar_kvempty + s, 1);
-    }
-    for (int s = 0; s < QS; ++s) {
-      mbar_init(bar_qfull + s, 1);
-      mbar_init(bar_qempty + s, 1);
-    }
-    for (int s = 0; s < DS; ++s) {
-      mbar_init(bar_dofull + s, 1);
-      mbar_init(bar_doempty + s, 1);
-    }
-    mbar_init(bar_sfull, 1);
-    mbar_init(bar_dpfull, 1);
-    mbar_init(bar_pready, 8);
-    mbar_init(bar_dsready, 8);
-    mbar_init(bar_dsfree, 1);
-    mbar_init(bar_dqfull, 1);
-    mbar_init(bar_dqfree, 4);
-    mbar_init(bar_accfull, 1);
-    mbar_init(bar_dvempty, 4);
-    mbar_init(bar_dkempty, 4);
-    mbar_init(bar_final, 1);
-    mbar_init(bar_dpfree, 8);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 9) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
-  grid_dep_launch();
-  const Watchdog wd{wait_limit, status, abort_flag};
-
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer (one lane)
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_do);
-      tma_prefetch_desc(&tm_dqacc);
-      int t = 0, q_issued = 0, do_issued = 0;
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int k = bwd_item_of(grid, r);
-        if (k < 0) break;
-        const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
-        if (x.n_iter == 0) continue;
-        const int kvs = t % KVS;
-        if (t >= KVS && !mbar_wait(bar_kvempty + kvs, ((t / KVS) - 1) & 1, wd)) break;
-        mbar_expect_tx(bar_kvfull + kvs, 2 * L::kTile);
-        uint8_t* kv = smem + L::kKV + kvs * 2 * L::kTile;
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_3d(kv + c * kChunk, &tm_k, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh);
-          tma_load_3d(kv + L::kTile + c * kChunk, &tm_v, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh);
-        }
-        ++t;
-        for (int it = 0, i = x.i0; it < x.n_iter; ++it, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
-          const int gq = q_issued, qs = gq % QS, ds = gq % DS;
-          if (gq >= QS && !mbar_wait(bar_qempty + qs, ((gq / QS) - 1) & 1, wd)) { ok = false; break; }
-          mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
-                        i * kBlock, x.bh);
-          const size_t roff = static_cast<size_t>(x.bh) * Npad + static_cast<size_t>(i) * kBlock;
-          bulk_load(smem + L::kStat + qs * 1024, lse2 + roff, 512, bar_qfull + qs);
-          bulk_load(smem + L::kStat + qs * 1024 + 512, delta + roff, 512, bar_qfull + qs);
-          q_issued = gq + 1;
-          if (gq >= DS && !mbar_wait(bar_doempty + ds, ((gq / DS) - 1) & 1, wd)) { ok = false; break; }
-          mbar_expect_tx(bar_dofull + ds, L::kTile);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
-                        i * kBlock, x.bh);
-          do_issued = gq + 1;
-        }
-      }
-      // Copies still in flight (only after an abort) must land before exit.
-      for (int u = max(0, t - KVS); u < t; ++u)
-        mbar_wait_drain(bar_kvfull + (u % KVS), (u / KVS) & 1, wait_limit);
-      for (int u = max(0, q_issued - QS); u < q_issued; ++u)
-        mbar_wait_drain(bar_qfull + (u % QS), (u / QS) & 1, wait_limit);
-      for (int u = max(0, do_issued - DS); u < do_issued; ++u)
-        mbar_wait_drain(bar_dofull + (u % DS), (u / DS) & 1, wait_limit);
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer (whole warp)
-    // On the critical path: the warp runs converged and an elected lane issues
-    // each tcgen05.mma / commit; it polls the barriers (test_wait) and fences
-    // only after the waits that follow tcgen05.ld / tcgen05.st of other
-    // threads (P^T ready, dS ready, dQ drained, dV/dK read out).
-    {
-      constexpr uint32_t kIdSS = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t kIdKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
-      constexpr uint32_t kIdMM = idesc_bf16(128, D, true, true);      // dQ: A, B MN-major
-      constexpr uint32_t kKVStride = 2 * L::kTile;
-      // Descriptors built once; per MMA only an offset is added.
-      const uint64_t k_kmaj0 = sdesc_sw128(smem_u32(smem + L::kKV), 16, 1024);
-      const uint64_t k_mn0 = sdesc_sw128(smem_u32(smem + L::kKV), kChunk, 1024);
-      const uint64_t v_kmaj0 = sdesc_sw128(smem_u32(smem + L::kKV + L::kTile), 16, 1024);
-      const uint64_t q_kmaj0 = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
-      const uint64_t q_mn0 = sdesc_sw128(smem_u32(smem + L::kQ), kChunk, 1024);
-      const uint64_t do_kmaj0 = sdesc_sw128(smem_u32(smem + L::kDO), 16, 1024);
-      const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + L::kDO), kChunk, 1024);
-      const uint64_t ds_kmaj = sdesc_sw128(smem_u32(smem + L::kDSb), 16, 1024);
-      const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + L::kDSb), kChunk, 1024);
-      using Cur = BwdCursor<CAUSAL, SPARSE>;
-      auto kv_ready = [&](const Cur& c) -> bool {
-        return mbar_wait_spin_w(bar_kvfull + (c.t % KVS), (c.t / KVS) & 1, wd);
-      };
-      auto issue_s = [&](const Cur& c) -> bool {
-        if (!mbar_wait_spin_w(bar_qfull + (c.g % QS), (c.g / QS) & 1, wd)) return false;
-        const uint64_t qd = desc_adv(q_kmaj0, (c.g % QS) * L::kTile);
-        const uint64_t kd = desc_adv(k_kmaj0, (c.t % KVS) * kKVStride);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss_w(tmem + L::kTS, desc_adv(kd, off), desc_adv(qd, off), kIdSS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(bar_sfull);
-        return true;
-      };
-      auto issue_dp = [&](const Cur& c) -> bool {
-        if (!mbar_wait_spin_w(bar_dofull + (c.g % DS), (c.g / DS) & 1, wd)) return false;
-        const uint64_t dd = desc_adv(do_kmaj0, (c.g % DS) * L::kTile);
-        const uint64_t vd = desc_adv(v_kmaj0, (c.t % KVS) * kKVStride);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-          mma_ss_w(tmem + L::kTDP, desc_adv(vd, off), desc_adv(dd, off), kIdSS, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(bar_dpfull);
-        return true;
-      };
-      Cur cur;
-      cur.seek(grid);
-      bool ok = cur.valid && kv_ready(cur) && issue_s(cur) && issue_dp(cur);
-      while (ok && cur.valid) {
-        Cur nx = cur;
-        nx.next(grid);
-        const int gq = cur.g;
-        const bool first = cur.it == 0, last = cur.it == cur.n - 1;
-        const uint64_t q_mn = desc_adv(q_mn0, (gq % QS) * L::kTile);
-        const uint64_t do_mn = desc_adv(do_mn0, (gq % DS) * L::kTile);
-        const uint64_t k_mn = desc_adv(k_mn0, (cur.t % KVS) * kKVStride);
-        const uint32_t acc0 = first ? 0u : 1u;
-        // dV += P^T dO: P^T (bf16) sits in the S^T columns [0,32) and [64,96)
-        if (!mbar_wait_spin_w(bar_pready, gq & 1, wd)) { ok = false; break; }
-        if (first && cur.t >= 1 && !mbar_wait_spin_w(bar_dvempty, (cur.t - 1) & 1, wd)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk) {
-          const uint32_t a_col = L::kTS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-          mma_ts_w(tmem + L::kTDV, tmem + a_col, desc_adv(do_mn, kk * 2048), kIdKM,
-                 kk > 0 ? 1u : acc0);
-        }
-        mma_commit_w(bar_doempty + (gq % DS));
-        // S^T of the next Q tile while dS of this one is formed. Across items
-        // with a single K/V stage it must wait until this item's dQ is issued.
-        const bool hoist = nx.valid && (KVS > 1 || !last);
-        if (hoist && !((nx.it > 0 || kv_ready(nx)) && issue_s(nx))) { ok = false; break; }
-        if (kEarlyDP && nx.valid) {  // hoist is true here: KVS > 1 at d = 64
-          if (!mbar_wait_spin_w(bar_dpfree, gq & 1, wd)) { ok = false; break; }
-          tc_fence_after();
-          if (!issue_dp(nx)) { ok = false; break; }
-        }
-        if (!mbar_wait_spin_w(bar_dsready, gq & 1, wd)) { ok = false; break; }
-        if (D == 64 && gq >= 1 && !mbar_wait_spin_w(bar_dqfree, (gq - 1) & 1, wd)) { ok = false; break; }
-        if (first && cur.t >= 1 && !mbar_wait_spin_w(bar_dkempty, (cur.t - 1) & 1, wd)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk) {
-          mma_ss_w(tmem + L::kTDK, desc_adv(ds_kmaj, (kk >> 2) * kChunk + (kk & 3) * 32),
-                 desc_adv(q_mn, kk * 2048), kIdKM, kk > 0 ? 1u : acc0);
-        }
-        mma_commit_w(bar_qempty + (gq % QS));
-#pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk) {
-          mma_ss_w(tmem + L::kTDQ, desc_adv(ds_mn, kk * 2048), desc_adv(k_mn, kk * 2048), kIdMM,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(bar_dqfull);
-        mma_commit_w(bar_dsfree);
-        if (last) {
-          mma_commit_w(bar_accfull);
-          mma_commit_w(bar_kvempty + (cur.t % KVS));
-        }
-        if (nx.valid) {
-          if (!hoist && !(kv_ready(nx) && issue_s(nx))) { ok = false; break; }
-          // d = 128: dQ occupies the dP^T columns until the drain warps have it
-          if (D == 128) {
-            if (!mbar_wait_spin_w(bar_dqfree, gq & 1, wd)) { ok = false; break; }
-            tc_fence_after();
-          }
-          if (!kEarlyDP && !issue_dp(nx)) { ok = false; break; }
-        }
-        cur = nx;
-      }
-      mma_commit_w(bar_final);
-      mbar_wait_drain(bar_final, 0, wait_limit);
-    }
-    __syncwarp();
-  } else if (warp >= 10) {
-    // ------------------------------------------------------------ dQ drain, dK/dV out (warps 10-13)
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;  // TMEM lane: query row of dQ, key row of dK / dV
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint8_t* stage = smem + L::kDQ;
-    const uint32_t st_base = smem_u32(stage);
-    const bool issuer = (quarter == 0 && lane == 0);
-    constexpr int kRounds = (D / 32) / L::kDQChunks;
-    int gq = 0, t = 0;
-    bool ok = true;
-    for (int r = 0; ok; ++r) {
-      const int k = bwd_item_of(grid, r);
-      if (k < 0) break;
-      const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
-      const int key = x.j * kBlock + row;
-      const size_t out_off = (static_cast<size_t>(x.bh) * N + key) * D;
-      if (x.n_iter == 0) {  // no valid key in this tile: zero gradients
-        if (key < N) {
-          uint4* a = reinterpret_cast<uint4*>(dk + out_off);
-          uint4* b = reinterpret_cast<uint4*>(dv + out_off);
-#pragma unroll
-          for (int u = 0; u < D / 8; ++u) {
-            a[u] = make_uint4(0u, 0u, 0u, 0u);
-            b[u] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        continue;
-      }
-      for (int it = 0, i = x.i0; it < x.n_iter; ++it, ++gq, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
-        if (!mbar_wait_warp(bar_dqfull, gq & 1, wd)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t v[D / 32][32];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + L::kTDQ + c * 32, v[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) reg_fence(v[c]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_dqfree);
-#pragma unroll
-        for (int round = 0; round < kRounds; ++round) {
-#pragma unroll
-          for (int cc = 0; cc < L::kDQChunks; ++cc) {
-            const int c = round * L::kDQChunks + cc;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint32_t addr = st_base + cc * kChunk + row * 128 + (((u ^ (row & 7))) << 4);
-              st_shared_v4(addr, __float_as_uint(__uint_as_float(v[c][4 * u + 0]) * scale),
-                           __float_as_uint(__uint_as_float(v[c][4 * u + 1]) * scale),
-                           __float_as_uint(__uint_as_float(v[c][4 * u + 2]) * scale),
-                           __float_as_uint(__uint_as_float(v[c][4 * u + 3]) * scale));
-            }
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(3, 128);
-          if (issuer) {
-#pragma unroll
-            for (int cc = 0; cc < L::kDQChunks; ++cc)
-              tma_reduce_add_3d(&tm_dqacc, stage + cc * kChunk, (round * L::kDQChunks + cc) * 32,
-                                i * kBlock, x.bh);
-            bulk_commit();
-            bulk_wait_read0();
-          }
-          named_bar_sync(3, 128);
-        }
-      }
-      if (!ok) break;
-      // dV (x1) and dK (x scale) of the item, straight from TMEM rows to HBM;
-      // each accumulator is released as soon as it has been read.
-      if (!mbar_wait_warp(bar_accfull, t & 1, wd)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? L::kTDV : L::kTDK;
-        const float mul = which == 0 ? 1.f : scale;
-        uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + out_off);
-#pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          uint32_t a[2][32];
-          tmem_ld32(lane_base + col + h * 64, a[0]);
-          tmem_ld32(lane_base + col + h * 64 + 32, a[1]);
-          tmem_wait_ld();
-          reg_fence(a[0]);
-          reg_fence(a[1]);
-          if (h == D / 64 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(which == 0 ? bar_dvempty : bar_dkempty);
-          }
-          if (key < N) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint32_t* s = &a[u >> 2][(u & 3) * 8];
-              dst[h * 8 + u] = make_uint4(
-                  pack_bf16(__uint_as_float(s[0]) * mul, __uint_as_float(s[1]) * mul),
-                  pack_bf16(__uint_as_float(s[2]) * mul, __uint_as_float(s[3]) * mul),
-                  pack_bf16(__uint_as_float(s[4]) * mul, __uint_as_float(s[5]) * mul),
-                  pack_bf16(__uint_as_float(s[6]) * mul, __uint_as_float(s[7]) * mul));
-            }
-          }
-        }
-      }
-      ++t;
-    }
-  } else {
-    // ------------------------------------------------------------ P / dS (warps 0-7)
-    const int wg = warp >> 2;             // query columns [64 wg, 64 wg + 64)
-    const int quarter = warp & 3;
-    const int kr = quarter * 32 + lane;   // key row within the tile == TMEM lane
-    const int qc0 = wg * 64;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t ds_base = smem_u32(smem + L::kDSb) + wg * kChunk;
-    int gq = 0;
-    bool ok = true;
-    for (int r = 0; ok; ++r) {
-      const int k = bwd_item_of(grid, r);
-      if (k < 0) break;
-      const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
-      const bool key_live = x.j * kBlock + kr < x.kv_bound;
-      for (int it = 0; it < x.n_iter; ++it, ++gq) {
-        const int s = gq % QS;
-        const int i = x.i0 + it;  // used only for the causal diagonal (dense)
-        const float* st_lse = reinterpret_cast<const float*>(smem + L::kStat + s * 1024) + qc0;
-        const float* st_delta = st_lse + 128;
-        if (!mbar_wait_warp(bar_qfull + s, (gq / QS) & 1, wd)) { ok = false; break; }
-        if (!mbar_wait_warp(bar_sfull, gq & 1, wd)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t rr[2][32];
-        tmem_ld32(lane_base + L::kTS + qc0, rr[0]);
-        tmem_ld32(lane_base + L::kTS + qc0 + 32, rr[1]);
-        tmem_wait_ld();
-        reg_fence(rr[0]);
-        reg_fence(rr[1]);
-        // P is kept only as bf16 pairs (the form the dV MMA consumes); dS below
-        // unpacks it, which halves the registers a compute thread holds.
-        const bool diag = CAUSAL && i == x.j;
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(st_lse + c);
-          float p0 = ex2(fmaf(__uint_as_float(rr[c >> 5][(c + 0) & 31]), scale_log2, -l4.x));
-          float p1 = ex2(fmaf(__uint_as_float(rr[c >> 5][(c + 1) & 31]), scale_log2, -l4.y));
-          float p2 = ex2(fmaf(__uint_as_float(rr[c >> 5][(c + 2) & 31]), scale_log2, -l4.z));
-          float p3 = ex2(fmaf(__uint_as_float(rr[c >> 5][(c + 3) & 31]), scale_log2, -l4.w));
-          if (diag) {  // query i*128+qc0+c < key j*128+kr
-            if (qc0 + c + 0 < kr) p0 = 0.f;
-            if (qc0 + c + 1 < kr) p1 = 0.f;
-            if (qc0 + c + 2 < kr) p2 = 0.f;
-            if (qc0 + c + 3 < kr) p3 = 0.f;
-          }
-          pk[c / 2] = key_live ? pack_bf16(p0, p1) : 0u;
-          pk[c / 2 + 1] = key_live ? pack_bf16(p2, p3) : 0u;
-        }
-        // P^T over the first 32 of this warpgroup's 64 S^T columns (already read)
-        tmem_st32(lane_base + L::kTS + qc0, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_pready);
-
-        if (!mbar_wait_warp(bar_dpfull, gq & 1, wd)) { ok = false; break; }
-        if (gq >= 1 && !mbar_wait_warp(bar_dsfree, (gq - 1) & 1, wd)) { ok = false; break; }
-        tc_fence_after();
-        tmem_ld32(lane_base + L::kTDP + qc0, rr[0]);
-        tmem_ld32(lane_base + L::kTDP + qc0 + 32, rr[1]);
-        tmem_wait_ld();
-        reg_fence(rr[0]);
-        reg_fence(rr[1]);
-        if constexpr (kEarlyDP) {  // dP^T may be overwritten by the next tile's now
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_dpfree);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int q0 = u * 8;
-          const float4 da = *reinterpret_cast<const float4*>(st_delta + q0);
-          const float4 db = *reinterpret_cast<const float4*>(st_delta + q0 + 4);
-          const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-          float gv[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t w = pk[(q0 + e) >> 1];
-            const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
-            gv[e] = pe * (__uint_as_float(rr[(q0 + e) >> 5][(q0 + e) & 31]) - dd[e]);
-          }
-          const uint32_t addr = ds_base + kr * 128 + (((u ^ (kr & 7))) << 4);
-          st_shared_v4(addr, pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),
-                       pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_dsready);
-      }
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 9) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
 
 __global__ void wait_selftest_kernel(int* status, long long limit) {
   __shared__ uint64_t bar;
@@ -759,7 +29,6 @@ int grid_for(long long threads) {
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
-  using L = BwdLayout<D>;
   const int BH = a.B * a.H;
   const int nt = (a.N + kBlock - 1) / kBlock;
   const int Npad = nt * kBlock;
@@ -771,21 +40,12 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageMain) {
-    auto kern = (!CAUSAL && a.block_mask != nullptr) ? bwd_main_kernel<D, false, true>
-                                                     : bwd_main_kernel<D, CAUSAL, false>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-    if (e != cudaSuccess) return e;
-    BwdGrid g;
-    g.H = a.H;
-    g.N = a.N;
-    g.nt = nt;
-    g.BH = BH;
-    g.n_items = BH * nt;
-    g.kv_len = a.kv_len;
-    g.mask = a.block_mask;
-    e = launch_pdl(kern, dim3(min(g.n_items, sm_count())), dim3(kThreads), L::kSmem, stream,
-                   a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g,
-                   Npad, a.scale, a.status, a.wait_limit);
+    if (a.drop.enabled)
+      e = launch_bwd_main_dropout(a, stream);
+    else if (!CAUSAL && a.block_mask != nullptr)
+      e = launch_bwd_main_t<D, false, true, false>(a, stream);
+    else
+      e = launch_bwd_main_t<D, CAUSAL, false, false>(a, stream);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageConvert) {

@@ -1,0 +1,20 @@
+// Backward main kernel with fused dropout (dense, causal, key-padded): the
+// DROP variants of fa_bwd_kernel.cuh. The keep decisions are regenerated from
+// the element indices with the forward pass's counter-based generator
+// (fa_philox.cuh), so the backward pass reads no mask. The preprocess and dQ
+// conversion stages are those of the pass without dropout: D = rowsum(dO * O)
+// still equals rowsum(P * dP) when O is formed from the dropped P.
+#include "fa_bwd_kernel.cuh"
+
+namespace fa {
+
+cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, cudaStream_t stream) {
+  const bool causal = a.causal != 0;
+  if (a.d == 64)
+    return causal ? launch_bwd_main_t<64, true, false, true>(a, stream)
+                  : launch_bwd_main_t<64, false, false, true>(a, stream);
+  return causal ? launch_bwd_main_t<128, true, false, true>(a, stream)
+                : launch_bwd_main_t<128, false, false, true>(a, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,762 @@
+// Forward pass of exact attention (dense, causal, key-padded and block-sparse)
+// as one fused sm_103a kernel.
+//
+// Method: FlashAttention's tiling with online softmax rescaling -- Q, K, V are
+// split into blocks that are copied from HBM into on-chip memory, attention is
+// computed block by block, the softmax normaliser is accumulated incrementally
+// and the N x N matrices S and P are never written to HBM (condensed paper
+// sample_paper.md, section 3 "Tiling" / "Softmax rescaling"; Medium article
+// "No More Quadratic Complexity for Transformers", Figure 1). The pages put
+// K/V in the outer loop; here each CTA keeps two 128-row Q tiles resident and
+// streams the K/V tiles past them, which gives the same exact result, keeps
+// the running statistics in registers and loads every K/V tile once for two
+// Q tiles.
+//
+// The kernel is persistent: one CTA per SM walks a list of work items (Q
+// tiles A = 2p and B = 2p + 1 of one (batch, head)); barrier phases continue
+// across items, so the next item's Q and K/V loads overlap the current one's
+// last steps and epilogue. 10 warps:
+//   warp 0      MMA issuer (below)
+//   warp 1      TMA producer: Q_A, Q_B per item; K_j, V_j through separate rings
+//   warps 2-5   softmax of tile A: each thread owns one query row, the TMEM
+//               lane of its warp's quarter (warp % 4)
+//   warps 6-9   softmax of tile B
+//   The MMA issuer runs, at d = 128, in the order
+//                 S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+//               so that the tensor core computes one tile's MMAs while the
+//               other tile's softmax runs.
+// TMEM columns: S_A [0,128), S_B [128,256) (fp32); O_A [256, 256+d),
+// O_B [256+d, 256+2d) (fp32 accumulators). The softmax writes P_t in bf16
+// pairs to TMEM and the PV MMA takes it from there as its A operand, so P never
+// touches shared memory. At d = 64, P_A and P_B have columns of their own
+// ([384,448), [448,512)): S_t(j+1) is then issued as soon as the softmax has
+// loaded S_t(j) into registers and is ready when P_t(j) is, and the issue
+// order becomes S_A(j+1) S_B(j+1) PV_A(j) PV_B(j). At d = 128 TMEM is full and
+// P_t goes over the first 64 columns of S_t. Each item ends with O / l stored
+// straight from TMEM to global memory, one row per thread.
+//
+// Rescaling is lazy: a row's reference maximum m only moves when the new
+// tile's maximum exceeds it by more than 8 (log2 units), so P <= 2^8 and O is
+// rescaled in TMEM only on those rare tiles; the final O / l is exact because
+// O and l always share the same m.
+//
+// An item pairs adjacent Q tiles, so both are active on (almost) every K/V
+// step and their softmax phases alternate on the tensor core; causal items
+// are handed out heaviest first, in a snake order across the CTAs.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
+#include "fa_internal.h"
+#include "fa_philox.cuh"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+// Warp roles: warp 0 issues MMAs (at d = 64 for Q tile slot A only, warp 2
+// for slot B), warp 1 issues TMA copies, then four softmax warps per slot.
+constexpr int kMmaWarp = 0, kLoadWarp = 1;
+template <int D>
+struct FwdWarps {
+  static constexpr int kMmaB = (D == 64) ? 2 : -1;  // second MMA issuer (d = 64)
+  static constexpr int kSoft0 = (D == 64) ? 3 : 2;  // first softmax warp
+  static constexpr int kThreads = (kSoft0 + 8) * 32;
+};
+constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled chunk (64 bf16 cols)
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
+
+template <int D>
+struct FwdLayout {
+  // d = 64 leaves TMEM room for P in columns of its own: the next S of a tile
+  // can then be computed while the softmax of the current one still runs.
+  static constexpr bool kSepP = (D == 64);
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = kChunks * kChunk;  // one 128 x D bf16 tile
+  static constexpr int kKS = 3;                   // K ring slots
+  static constexpr int kVS = (D == 128) ? 2 : 3;  // V ring slots
+  static constexpr int kQS = (D == 128) ? 1 : 2;  // Q stages per tile slot
+  static constexpr int kQ = 0;                    // Q of slot t, stage s: kQ + (t kQS + s) kTile
+  static constexpr int kK = kQ + 2 * kQS * kTile;
+  static constexpr int kV = kK + kKS * kTile;
+  static constexpr int kBar = kV + kVS * kTile;
+  static constexpr int kEnd = kBar + 256;
+  static constexpr int kSmem = kEnd + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t kTO = 256;       // O_A; O_B at kTO + D
+  // P_t (bf16 pairs, 64 columns): its own columns, or over the first 64 of S_t
+  static constexpr uint32_t kTP = kSepP ? 256 + 2 * D : 0;
+  __host__ __device__ static constexpr uint32_t p_col(int t) { return kSepP ? kTP + t * 64 : t * 128; }
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Which K/V tiles a Q tile visits: j < end, and the block-mask bit if any.
+struct TileSet {
+  int end;
+  const uint8_t* mrow;
+  __device__ bool has(int j) const { return j < end && (mrow == nullptr || mrow[j] != 0); }
+  __device__ int last() const {  // last visited tile, -1 if none
+    int j = end - 1;
+    if (mrow != nullptr)
+      while (j >= 0 && mrow[j] == 0) --j;
+    return j;
+  }
+};
+
+// One work item: Q tiles 2p and 2p+1 (B = -1 if absent) of one (batch, head).
+struct FwdItem {
+  int bh, qtA, qtB, kv_bound, uend;
+  TileSet tsA, tsB;
+};
+
+struct FwdGrid {
+  int H, N, nqt, npairs, n_items;
+  const int32_t* kv_len;
+  const uint8_t* block_mask;
+};
+
+// Item k. Causal items are ordered heaviest first (pairs near the diagonal end
+// see the most K/V tiles); otherwise a head's pairs are consecutive.
+template <bool CAUSAL>
+__device__ FwdItem make_item(const FwdGrid& g, int k) {
+  FwdItem it;
+  const int BH = g.n_items / g.npairs;
+  int p;
+  if (CAUSAL) {
+    p = g.npairs - 1 - k / BH;
+    it.bh = k % BH;
+  } else {
+    it.bh = k / g.npairs;
+    p = k % g.npairs;
+  }
+  it.qtA = 2 * p;
+  it.qtB = 2 * p + 1 < g.nqt ? 2 * p + 1 : -1;
+  it.kv_bound = g.N;
+  if (g.kv_len != nullptr) it.kv_bound = min(g.N, max(0, g.kv_len[it.bh / g.H]));
+  const int kv_tiles = (it.kv_bound + kBlock - 1) / kBlock;
+  it.tsA.end = CAUSAL ? min(kv_tiles, it.qtA + 1) : kv_tiles;
+  it.tsA.mrow = g.block_mask != nullptr ? g.block_mask + static_cast<size_t>(it.qtA) * g.nqt : nullptr;
+  it.tsB.end = it.qtB < 0 ? 0 : (CAUSAL ? min(kv_tiles, it.qtB + 1) : kv_tiles);
+  it.tsB.mrow = (g.block_mask != nullptr && it.qtB >= 0)
+                    ? g.block_mask + static_cast<size_t>(it.qtB) * g.nqt
+                    : nullptr;
+  it.uend = max(it.tsA.end, it.tsB.end);
+  return it;
+}
+
+// The r-th item of this CTA: a snake over the (heaviest-first) item list, so
+// that every CTA gets a similar amount of work; -1 when there is none.
+__device__ __forceinline__ int item_of(const FwdGrid& g, int r) {
+  const int G = gridDim.x, c = blockIdx.x;
+  if (r * G >= g.n_items) return -1;
+  const int k = r * G + ((r & 1) ? G - 1 - c : c);
+  return k < g.n_items ? k : -1;  // only the last round can run past the end
+}
+
+// DROP: inverted dropout on P (fa_philox.cuh); the row sums and LSE use the
+// undropped P, the PV product the dropped one, and O is scaled by 1 / (1 - p').
+template <int D, bool CAUSAL, bool DROP>
+__global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+               float* __restrict__ lse_out, FwdGrid g, float scale_log2, DropoutParams dp,
+               int* status, long long wait_limit) {
+  using L = FwdLayout<D>;
+  constexpr int KS = L::kKS, VS = L::kVS, QS = L::kQS;
+  constexpr bool kSepP = L::kSepP;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* bar_qfull = bars + 0;    // [2][QS] per Q slot (A, B) and stage
+  uint64_t* bar_qempty = bars + 4;   // [2][QS]
+  uint64_t* bar_kfull = bars + 8;    // [KS]
+  uint64_t* bar_kempty = bars + 11;  // [KS]
+  uint64_t* bar_vfull = bars + 14;   // [VS]
+  uint64_t* bar_vempty = bars + 17;  // [VS]
+  uint64_t* bar_sfull = bars + 20;   // [2]
+  uint64_t* bar_pfull = bars + 22;   // [2]
+  uint64_t* bar_odone = bars + 24;   // [2]
+  uint64_t* bar_sfree = bars + 26;   // [2] S_t read out of TMEM (separate-P layout)
+  uint64_t* bar_final = bars + 28;   // [2] one per MMA issuer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
+  int* abort_flag = reinterpret_cast<int*>(bars + 31);
+  constexpr int kMmaB = FwdWarps<D>::kMmaB, kSoft0 = FwdWarps<D>::kSoft0;
+  constexpr int kIssuers = kSepP ? 2 : 1;  // arrivals that release a K or V ring slot
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      for (int q = 0; q < QS; ++q) {
+        mbar_init(bar_qfull + t * QS + q, 1);
+        mbar_init(bar_qempty + t * QS + q, 1);
+      }
+      mbar_init(bar_sfull + t, 1);
+      mbar_init(bar_pfull + t, 4);
+      mbar_init(bar_odone + t, 1);
+      mbar_init(bar_sfree + t, 4);
+    }
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(bar_kfull + s, 1);
+      mbar_init(bar_kempty + s, kIssuers);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(bar_vfull + s, 1);
+      mbar_init(bar_vempty + s, kIssuers);
+    }
+    mbar_init(bar_final, 1);
+    mbar_init(bar_final + 1, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
+  grid_dep_launch();
+  const Watchdog wd{wait_limit, status, abort_flag};
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer (one lane)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int nqA = 0, nqB = 0;  // Q loads issued per slot
+      int k_issued = 0, v_issued = 0;
+      int u = 0;           // position in the K/V rings, continued across items
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int k = item_of(g, r);
+        if (k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, k);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if ((t ? it.tsB : it.tsA).last() < 0) continue;
+          int& nq = t ? nqB : nqA;
+          const int qb = t * QS + nq % QS;
+          if (nq >= QS && !mbar_wait(bar_qempty + qb, ((nq / QS) - 1) & 1, wd)) { ok = false; break; }
+          mbar_expect_tx(bar_qfull + qb, L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kQ + qb * L::kTile + c * kChunk, &tm_q, bar_qfull + qb, c * 64,
+                        (t ? it.qtB : it.qtA) * kBlock, it.bh);
+          ++nq;
+        }
+        for (int j = 0; ok && j < it.uend; ++j) {
+          if (!it.tsA.has(j) && !it.tsB.has(j)) continue;
+          const int ks = u % KS, vs = u % VS;
+          if (u >= KS && !mbar_wait(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) { ok = false; break; }
+          mbar_expect_tx(bar_kfull + ks, L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
+                        j * kBlock, it.bh);
+          k_issued = u + 1;
+          if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) { ok = false; break; }
+          mbar_expect_tx(bar_vfull + vs, L::kTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
+                        j * kBlock, it.bh);
+          v_issued = u + 1;
+          ++u;
+        }
+      }
+      // Let every copy in flight land before the CTA can exit (bounded).
+      for (int t = 0; t < 2; ++t) {
+        const int nq = t ? nqB : nqA;
+        for (int q = max(0, nq - QS); q < nq; ++q)
+          mbar_wait_drain(bar_qfull + t * QS + q % QS, (q / QS) & 1, wait_limit);
+      }
+      for (int t = max(0, k_issued - KS); t < k_issued; ++t)
+        mbar_wait_drain(bar_kfull + (t % KS), (t / KS) & 1, wait_limit);
+      for (int t = max(0, v_issued - VS); t < v_issued; ++t)
+        mbar_wait_drain(bar_vfull + (t % VS), (t / VS) & 1, wait_limit);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp || warp == kMmaB) {
+    // ------------------------------------------------------------ MMA issuers (whole warps)
+    // An issuer sits on the critical path between the softmax warpgroups. The
+    // warp runs converged and an elected lane issues each tcgen05.mma /
+    // commit; it polls the barriers and places a tcgen05 fence only after
+    // waiting on another thread's TMEM access (P_t written by tcgen05.st; S_t
+    // read by tcgen05.ld before S_t(j+1) overwrites it).
+    if constexpr (kSepP) {
+      // d = 64: one issuer per Q tile slot X, each walking every K/V tile of
+      // its items. Both release each K and V ring slot (count 2): with an MMA
+      // commit when slot X used the tile, else with a plain arrive once the
+      // tile is known to be loaded, which keeps the ring's phases in order.
+      const int X = (warp == kMmaWarp) ? 0 : 1;
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
+      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);     // K-major
+      const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
+      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
+      const uint32_t s_tm = tmem + X * 128, o_tm = tmem + L::kTO + X * D;
+      const uint32_t p_tm = tmem + L::p_col(X);
+      uint64_t* my_sfull = bar_sfull + X;
+      uint64_t* my_sfree = bar_sfree + X;
+      uint64_t* my_pfull = bar_pfull + X;
+      uint64_t* my_odone = bar_odone + X;
+      int npv = 0, nq = 0, ns = 0;  // P V MMAs, Q tiles, S tiles of this slot so far
+      int u = 0;                    // position in the K/V rings
+      int k_ready = -1, v_ready = -1;  // ring positions already seen loaded
+      bool ok = true;
+      auto k_wait = [&](int uu) -> bool {
+        if (uu == k_ready) return true;
+        if (!mbar_wait_spin_w(bar_kfull + (uu % KS), (uu / KS) & 1, wd)) return false;
+        k_ready = uu;
+        return true;
+      };
+      auto v_wait = [&](int uu) -> bool {
+        if (uu == v_ready) return true;
+        if (!mbar_wait_spin_w(bar_vfull + (uu % VS), (uu / VS) & 1, wd)) return false;
+        v_ready = uu;
+        return true;
+      };
+      for (int r = 0; ok; ++r) {
+        const int k = item_of(g, r);
+        if (k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, k);
+        const TileSet my = X ? it.tsB : it.tsA;
+        const int last = my.last();
+        bool needq = last >= 0;
+        int loc = 0;  // P V MMAs of this item
+        const int qb = X * QS + nq % QS;
+        auto issue_s = [&](int uu, int j) -> bool {
+          if (needq) {
+            if (!mbar_wait_spin_w(bar_qfull + qb, (nq / QS) & 1, wd)) return false;
+            needq = false;
+          }
+          if (!k_wait(uu)) return false;
+          if (ns >= 1) {  // the softmax has read S_X(previous) out of TMEM
+            if (!mbar_wait_spin_w(my_sfree, (ns - 1) & 1, wd)) return false;
+            tc_fence_after();
+          }
+          ++ns;
+          const uint64_t qd = desc_adv(q_desc, qb * L::kTile);
+          const uint64_t kd = desc_adv(k_desc, (uu % KS) * L::kTile);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            mma_ss_w(s_tm, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_w(my_sfull);
+          if (j == last) {  // Q_X of this item is no longer needed
+            mma_commit_w(bar_qempty + qb);
+            ++nq;
+          }
+          return true;
+        };
+        auto issue_pv = [&](int uu) -> bool {
+          if (!mbar_wait_spin_w(my_pfull, npv & 1, wd)) return false;
+          if (!v_wait(uu)) return false;
+          tc_fence_after();
+          const uint64_t vd = desc_adv(v_desc, (uu % VS) * L::kTile);
+          const uint32_t acc0 = loc > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < kBlock / 16; ++kk)
+            mma_ts_w(o_tm, p_tm + kk * 8, desc_adv(vd, kk * 2048), kIdO, kk > 0 ? 1u : acc0);
+          mma_commit_w(my_odone);
+          ++npv;
+          ++loc;
+          return true;
+        };
+        auto release_k = [&](int uu, bool used) -> bool {
+          if (used) {
+            mma_commit_w(bar_kempty + (uu % KS));
+            return true;
+          }
+          if (!k_wait(uu)) return false;
+          mbar_arrive_w(bar_kempty + (uu % KS));
+          return true;
+        };
+        auto release_v = [&](int uu, bool used) -> bool {
+          if (used) {
+            mma_commit_w(bar_vempty + (uu % VS));
+            return true;
+          }
+          if (!v_wait(uu)) return false;
+          mbar_arrive_w(bar_vempty + (uu % VS));
+          return true;
+        };
+        int j = 0;
+        while (j < it.uend && !it.tsA.has(j) && !it.tsB.has(j)) ++j;
+        if (j >= it.uend) continue;
+        {
+          const bool h = my.has(j);
+          if (h) ok = issue_s(u, j);
+          if (ok) ok = release_k(u, h);
+        }
+        while (ok && j < it.uend) {
+          int jn = j + 1;
+          while (jn < it.uend && !it.tsA.has(jn) && !it.tsB.has(jn)) ++jn;
+          const int un = u + 1;
+          // S_X(j+1) as soon as the softmax has read S_X(j), then P_X(j) V_j
+          if (jn < it.uend) {
+            const bool h = my.has(jn);
+            if (h) ok = issue_s(un, jn);
+            if (ok) ok = release_k(un, h);
+          }
+          if (ok) {
+            const bool h = my.has(j);
+            if (h) ok = issue_pv(u);
+            if (ok) ok = release_v(u, h);
+          }
+          j = jn;
+          u = un;
+        }
+      }
+      mma_commit_w(bar_final + X);
+      mbar_wait_drain(bar_final + X, 0, wait_limit);
+    } else {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
+      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
+      // Descriptors built once; per MMA only a compile-time offset is added.
+      const uint64_t q_desc = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);     // K-major
+      const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
+      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
+      // Per-slot state is kept in scalars and slots are compile-time constants
+      // (generic lambdas over std::integral_constant), so nothing of this hot
+      // loop lives in local memory.
+      int npvA = 0, npvB = 0;  // P V MMAs issued per slot (pfull / odone phases)
+      int nqA = 0, nqB = 0;    // Q tiles consumed per slot (qfull phases)
+      int nsA = 0, nsB = 0;    // S tiles issued per slot (sfree phases)
+      int u = 0;               // position in the K/V rings
+      bool ok = true;
+      using SlotA = std::integral_constant<int, 0>;
+      using SlotB = std::integral_constant<int, 1>;
+      for (int r = 0; ok; ++r) {
+        const int k = item_of(g, r);
+        if (k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, k);
+        const int lastA = it.tsA.last(), lastB = it.tsB.last();
+        bool needqA = lastA >= 0, needqB = lastB >= 0;
+        int locA = 0, locB = 0;  // P V MMAs of this item per slot
+        auto issue_s = [&](auto slot, int uu, int j) -> bool {
+          constexpr int t = decltype(slot)::value;
+          bool& needq = t ? needqB : needqA;
+          int& nq = t ? nqB : nqA;
+          int& ns = t ? nsB : nsA;
+          const int qb = t * QS + nq % QS;
+          if (needq) {
+            if (!mbar_wait_spin_w(bar_qfull + qb, (nq / QS) & 1, wd)) return false;
+            needq = false;
+          }
+          if (!mbar_wait_spin_w(bar_kfull + (uu % KS), (uu / KS) & 1, wd)) return false;
+          if (kSepP && ns >= 1) {  // the softmax has read S_t(previous) out of TMEM
+            if (!mbar_wait_spin_w(bar_sfree + t, (ns - 1) & 1, wd)) return false;
+            tc_fence_after();
+          }
+          ++ns;
+          const uint64_t qd = desc_adv(q_desc, qb * L::kTile);
+          const uint64_t kd = desc_adv(k_desc, (uu % KS) * L::kTile);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
+            mma_ss_w(tmem + t * 128, desc_adv(qd, off), desc_adv(kd, off), kIdS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_w(bar_sfull + t);
+          if (j == (t ? lastB : lastA)) {  // Q_t of this item is no longer needed
+            mma_commit_w(bar_qempty + qb);
+            ++nq;
+          }
+          return true;
+        };
+        auto issue_pv = [&](auto slot, int uu) -> bool {
+          constexpr int t = decltype(slot)::value;
+          int& npv = t ? npvB : npvA;
+          int& loc = t ? locB : locA;
+          if (!mbar_wait_spin_w(bar_pfull + t, npv & 1, wd)) return false;
+          if (!mbar_wait_spin_w(bar_vfull + (uu % VS), (uu / VS) & 1, wd)) return false;
+          tc_fence_after();
+          const uint64_t vd = desc_adv(v_desc, (uu % VS) * L::kTile);
+          const uint32_t acc0 = loc > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < kBlock / 16; ++kk) {
+            // A = P_t (bf16 pairs, from TMEM), B = V, MN-major.
+            mma_ts_w(tmem + L::kTO + t * D, tmem + L::p_col(t) + kk * 8, desc_adv(vd, kk * 2048), kIdO,
+                   kk > 0 ? 1u : acc0);
+          }
+          mma_commit_w(bar_odone + t);
+          ++npv;
+          ++loc;
+          return true;
+        };
+        int j = 0;
+        while (j < it.uend && !it.tsA.has(j) && !it.tsB.has(j)) ++j;
+        if (j >= it.uend) continue;
+        if (it.tsA.has(j)) ok = issue_s(SlotA{}, u, j);
+        if (ok && it.tsB.has(j)) ok = issue_s(SlotB{}, u, j);
+        if (ok) mma_commit_w(bar_kempty + (u % KS));
+        while (ok && j < it.uend) {
+          int jn = j + 1;
+          while (jn < it.uend && !it.tsA.has(jn) && !it.tsB.has(jn)) ++jn;
+          const int un = u + 1;
+          if constexpr (kSepP) {
+            // S_t(j+1) as soon as the softmax has read S_t(j), so that it is
+            // ready when P_t(j) is; then P_A(j) V_j and P_B(j) V_j.
+            if (jn < it.uend) {
+              if (it.tsA.has(jn)) ok = issue_s(SlotA{}, un, jn);
+              if (ok && it.tsB.has(jn)) ok = issue_s(SlotB{}, un, jn);
+              if (ok) mma_commit_w(bar_kempty + (un % KS));
+            }
+            if (ok && it.tsA.has(j)) ok = issue_pv(SlotA{}, u);
+            if (ok && it.tsB.has(j)) ok = issue_pv(SlotB{}, u);
+            if (ok) mma_commit_w(bar_vempty + (u % VS));
+          } else {
+            // tile A: P_A(j) V_j, then S_A(j+1) over the columns P_A(j) just left
+            if (it.tsA.has(j)) ok = issue_pv(SlotA{}, u);
+            if (ok && jn < it.uend && it.tsA.has(jn)) ok = issue_s(SlotA{}, un, jn);
+            if (ok && it.tsB.has(j)) ok = issue_pv(SlotB{}, u);
+            if (ok) mma_commit_w(bar_vempty + (u % VS));
+            if (ok && jn < it.uend && it.tsB.has(jn)) ok = issue_s(SlotB{}, un, jn);
+            if (ok && jn < it.uend) mma_commit_w(bar_kempty + (un % KS));
+          }
+          j = jn;
+          u = un;
+        }
+      }
+      mma_commit_w(bar_final);
+      mbar_wait_drain(bar_final, 0, wait_limit);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int t = (warp - kSoft0) >> 2;  // which Q slot
+    const int r = (warp & 3) * 32 + lane;     // row within the tile == TMEM lane (quarter warp % 4)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_col = t * 128;
+    const uint32_t p_col = L::p_col(t);
+    const uint32_t o_col = L::kTO + t * D;
+    int ns = 0;  // S tiles of this slot consumed so far (sfull / pfull / odone phases)
+    bool ok = true;
+    for (int ri = 0; ok; ++ri) {
+      const int k = item_of(g, ri);
+      if (k < 0) break;
+      const FwdItem it = make_item<CAUSAL>(g, k);
+      const int qt = t ? it.qtB : it.qtA;
+      if (qt < 0) continue;
+      const TileSet my = t ? it.tsB : it.tsA;
+      const int kv_bound = it.kv_bound;
+      const int row = qt * kBlock + r;
+      float m = -INFINITY;  // reference max, log2 units (scale folded in)
+      float l = 0.f;        // sum of exp2(s * scale_log2 - m) over visited keys
+      int n = 0;            // tiles of this item
+      for (int j = 0; j < my.end; ++j) {
+        if (!my.has(j)) continue;
+        if (!mbar_wait_warp<true>(bar_sfull + t, ns & 1, wd)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t rs[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, rs[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence(rs[c]);
+        if constexpr (kSepP) {  // S_t may be overwritten by the next tile's S now
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sfree + t);
+        }
+        float sv[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(rs[c >> 5][c & 31]);
+        if ((j + 1) * kBlock > kv_bound || (CAUSAL && j == qt)) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const int key = j * kBlock + c;
+            if (key >= kv_bound || (CAUSAL && key > row)) sv[c] = -INFINITY;
+          }
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = max3(sv[i], sv[i + 8], sv[i + 16]);
+#pragma unroll
+        for (int c = 24; c < 128; c += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mx[i] = (c + 8 + i < 128) ? max3(mx[i], sv[c + i], sv[c + 8 + i]) : fmaxf(mx[i], sv[c + i]);
+        }
+        const float tmax =
+            max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+            scale_log2;
+        const bool grow = tmax > m + kRescaleThreshold;
+        const float m_new = grow ? tmax : m;
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = grow ? ex2(m - m_use) : 1.f;
+        if (kSepP && n >= 1) {
+          // P_t's columns are free (and O quiescent) once this item's previous P V is done.
+          if (!mbar_wait_warp<true>(bar_odone + t, (ns - 1) & 1, wd)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        // P_t (bf16 pairs) goes to TMEM 16 columns at a time as soon as it is
+        // formed -- in its own columns, or over the first 64 columns of S_t,
+        // whose fp32 values are already in registers -- so that few packed
+        // words are live at once.
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float p0 = ex2(fmaf(sv[2 * (c0 + c)], scale_log2, -m_use));
+            const float p1 = ex2(fmaf(sv[2 * (c0 + c) + 1], scale_log2, -m_use));
+            pk[c] = pack_bf16(p0, p1);
+            ps[c & 3] += p0 + p1;
+          }
+          if constexpr (DROP) {
+            // keys j*128 + 2*c0 + [0, 32): two Philox blocks of 16 keep bytes
+            const uint32_t grp = static_cast<uint32_t>(j * kBlock + 2 * c0) >> 4;
+            const uint4 ra = philox4x32_10(grp, row, it.bh, dp.offset, dp.k0, dp.k1);
+            const uint4 rb = philox4x32_10(grp + 1, row, it.bh, dp.offset, dp.k0, dp.k1);
+            const uint32_t km[8] = {keep_bytes(ra.x, dp.thresh4), keep_bytes(ra.y, dp.thresh4),
+                                    keep_bytes(ra.z, dp.thresh4), keep_bytes(ra.w, dp.thresh4),
+                                    keep_bytes(rb.x, dp.thresh4), keep_bytes(rb.y, dp.thresh4),
+                                    keep_bytes(rb.z, dp.thresh4), keep_bytes(rb.w, dp.thresh4)};
+#pragma unroll
+            for (int c = 0; c < 16; ++c) pk[c] &= pair_mask(km[c >> 1], c & 1);
+          }
+          tmem_st16(lane_base + p_col + c0, pk);
+        }
+        const float tsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        if (n >= 1 && __any_sync(0xffffffffu, grow)) {
+          // O must be quiescent (this item's previous P V done) before it is rescaled.
+          if (!kSepP) {
+            if (!mbar_wait_warp<true>(bar_odone + t, (ns - 1) & 1, wd)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < D / 32; ++c0) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + o_col + c0 * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(lane_base + o_col + c0 * 32, o);
+          }
+        }
+        tmem_wait_st();
+        l = l * alpha + tsum;
+        m = m_new;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pfull + t);
+        ++n;
+        ++ns;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------- epilogue
+      // O / l straight from TMEM to global memory (one row per thread); the
+      // next item's first P V overwrites O only after this thread's next P
+      // arrives, i.e. after these loads.
+      bool have = n > 0;
+      if (have) {
+        if (!mbar_wait_warp<true>(bar_odone + t, (ns - 1) & 1, wd)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const bool live = have && l > 0.f;
+      const float inv = live ? (DROP ? dp.rescale : 1.f) / l : 0.f;
+      const bool row_ok = row < g.N;
+      uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(it.bh) * g.N + row) * D);
+#pragma unroll
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t o[32];
+        if (have) {
+          tmem_ld32(lane_base + o_col + c0 * 32, o);
+          tmem_wait_ld();
+          reg_fence(o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+            orow[c0 * 4 + v] = w;
+          }
+        }
+      }
+      if (row_ok)
+        lse_out[static_cast<size_t>(it.bh) * g.N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL, bool DROP>
+cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+  using L = FwdLayout<D>;
+  auto kern = fwd_kernel<D, CAUSAL, DROP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  FwdGrid g;
+  g.H = a.H;
+  g.N = a.N;
+  g.nqt = (a.N + kBlock - 1) / kBlock;
+  g.npairs = (g.nqt + 1) / 2;
+  g.n_items = a.B * a.H * g.npairs;
+  g.kv_len = a.kv_len;
+  g.block_mask = a.block_mask;
+  const int grid = min(g.n_items, sm_count());
+  const float scale_log2 = a.scale * 1.4426950408889634f;
+  return launch_pdl(kern, dim3(grid), dim3(FwdWarps<D>::kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
+                    a.o, a.lse, g, scale_log2, a.drop, a.status, a.wait_limit);
+}
+
+}  // namespace
+}  // namespace fa

@@ -15,6 +15,18 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 // Rows of one Q tile and one K/V tile (the 128 x 128 block of the method).
 constexpr int kBlock = 128;
 
+// Dropout on the attention probabilities (inverted: kept entries are scaled
+// by 1 / (1 - p')). Element (b, h, i, j) draws byte j mod 16 of the
+// Philox4x32-10 block at counter (j / 16, i, b*H + h, offset) under key
+// (k0, k1); it is kept iff that byte >= thresh (p' = thresh / 256).
+struct DropoutParams {
+  uint32_t k0, k1;    // seed low / high 32 bits
+  uint32_t offset;    // fourth counter word
+  uint32_t thresh4;   // thresh replicated into the four bytes
+  float rescale;      // 256 / (256 - thresh)
+  int enabled;        // 0: no dropout (the other fields are ignored)
+};
+
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H, N, d], box 64 x 128 x 1, 128B swizzle
   void* o;
@@ -24,6 +36,7 @@ struct FwdLaunch {
   float scale;
   const int32_t* kv_len;      // device [B] or nullptr
   const uint8_t* block_mask;  // device [nb, nb] or nullptr
+  DropoutParams drop;
   int* status;
   long long wait_limit;
 };
@@ -45,6 +58,7 @@ struct BwdLaunch {
   float* lse2;     // workspace: fp32 [B*H, Npad]  (LSE * log2 e; +inf on padding rows)
   float* delta;    // workspace: fp32 [B*H, Npad]  (rowsum(dO * O); 0 on padding rows)
   const uint8_t* block_mask;  // device [nt][nt] (block-sparse backward) or nullptr
+  DropoutParams drop;
   int* status;
   long long wait_limit;
 };
@@ -81,6 +95,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
+// The dropout variants (a.drop.enabled != 0), compiled in their own
+// translation units: the forward kernel and the backward main kernel.
+cudaError_t launch_fwd_dropout(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, cudaStream_t stream);
+// Writes the keep decisions Z (1 = kept) of a.drop for [B*H, N, N] as bytes.
+cudaError_t launch_dropout_mask(const DropoutParams& drop, int BH, int N, uint8_t* keep,
+                                cudaStream_t stream);
 // Backward stages (bit set): preprocess, main kernel, dQ conversion.
 constexpr int kBwdStagePre = 1, kBwdStageMain = 2, kBwdStageConvert = 4, kBwdStageAll = 7;
 cudaError_t launch_bwd(const BwdLaunch& a, int stages, cudaStream_t stream);

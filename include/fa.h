@@ -1,6 +1,7 @@
 /*
  * fa.h -- C-ABI of libfa.so: exact scaled-dot-product attention on one
- * GB300 (sm_103a), forward, backward and block-sparse forward.
+ * GB300 (sm_103a): forward and backward, dense, causal, key-padded,
+ * block-sparse and with fused dropout.
  *
  * What is computed (per batch b and head h; Q, K, V, dO in R^{N x d}):
  *   S = scale * Q K^T + M,  P = softmax(S) row-wise,  O = P V,
@@ -165,6 +166,46 @@ int fa_blocksparse_bwd(const void* q, const void* k, const void* v, const void* 
                        const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
                        int H, int N, int d, float scale, const uint8_t* block_mask, int block_size,
                        void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/* Attention with fused dropout on P (inverted dropout): O = (P * Z / (1 - p')) V
+ * with Z_ij in {0, 1}, LSE that of the undropped scores. Dropout is one of the
+ * stages that the method fuses into its single kernel, at no extra memory
+ * (FlashAttention aggregator page, GPT-2 time-breakdown figure); the keep
+ * decisions are drawn on chip and never stored, and the backward pass draws
+ * them again from the same indices.
+ *   Draws: Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as
+ *   1, 2, 3", SC'11) with key (seed mod 2^32, seed div 2^32). Element
+ *   (b, h, i, j) uses byte j mod 16 (byte j mod 4 of word (j mod 16) / 4,
+ *   little-endian) of the block at counter (j / 16, i, b*H + h, offset), and
+ *   is kept iff that byte >= t, t = round(256 * dropout_p) capped at 255, so
+ *   the drop probability is p' = t / 256 and kept entries are scaled by
+ *   256 / (256 - t). Use a new (seed, offset) pair for every call whose mask
+ *   must be independent of earlier ones.
+ *   dropout_p : in [0, 1) (else FA_ERR_INVALID_ARG); 0 gives fa_fwd's result.
+ * Other arguments, layouts and errors: as fa_fwd_kpad (kv_len may be NULL). */
+int fa_dropout_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int N, int d, int causal, float scale, const int32_t* kv_len,
+                   float dropout_p, uint64_t seed, uint32_t offset, struct CUstream_st* stream);
+
+/* Backward pass of fa_dropout_fwd: gradients of L = sum(dO * O) with the same
+ * (dropout_p, seed, offset) -- dV = Pd^T dO with Pd = P * Z / (1 - p'), and
+ * dS = P * (Z * dPd / (1 - p') - D), dPd = dO V^T, D = rowsum(dO * O).
+ * Arguments, workspace and errors: as fa_bwd (o and lse from fa_dropout_fwd
+ * with the same causal, scale, kv_len, dropout_p, seed and offset). */
+int fa_dropout_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, const int32_t* kv_len, float dropout_p, uint64_t seed,
+                   uint32_t offset, void* workspace, size_t workspace_bytes,
+                   struct CUstream_st* stream);
+
+/* The keep decisions Z of fa_dropout_fwd / fa_dropout_bwd for the same
+ * (B, H, N, dropout_p, seed, offset): keep is a DEVICE uint8 [B, H, N, N]
+ * (query row i, key j), 1 where the element is kept, 0 where it is dropped.
+ * For inspection and tests; the attention calls never materialise it.
+ * Errors: FA_ERR_INVALID_ARG for B, H or N < 1, a NULL keep or dropout_p
+ * outside [0, 1). */
+int fa_dropout_mask(int B, int H, int N, float dropout_p, uint64_t seed, uint32_t offset,
+                    uint8_t* keep, struct CUstream_st* stream);
 
 /* Device-side status of the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT
  * if a bounded wait inside a kernel gave up since the last call. Reading

@@ -5,6 +5,8 @@ Tolerances (bf16 inputs, fp32 accumulation on the GPU):
   O      max-abs error            <= 1e-2
   LSE    max-abs error            <= 1e-3   (-inf must match -inf exactly)
   dQ/dK/dV  max-abs error / max-abs of the oracle gradient <= 2e-2 per tensor
+With dropout the O and gradient bars are multiplied by the rescale factor
+r = 1 / (1 - p') (see tests/test_gpu_dropout.py).
 """
 import numpy as np
 import torch
@@ -34,9 +36,9 @@ def fwd_errors(o_gpu, lse_gpu, o_ref, lse_ref):
     return err_o, err_l
 
 
-def check_fwd(o_gpu, lse_gpu, o_ref, lse_ref, tag=""):
+def check_fwd(o_gpu, lse_gpu, o_ref, lse_ref, tag="", o_atol=O_ATOL):
     err_o, err_l = fwd_errors(o_gpu, lse_gpu, o_ref, lse_ref)
-    assert err_o <= O_ATOL, f"{tag} O max-abs error {err_o:.3e}"
+    assert err_o <= o_atol, f"{tag} O max-abs error {err_o:.3e}"
     assert err_l <= LSE_ATOL, f"{tag} LSE max-abs error {err_l:.3e}"
     return err_o, err_l
 
@@ -49,10 +51,10 @@ def grad_rel(g, ref) -> float:
     return err / scale if scale > 0 else err
 
 
-def check_grads(grads_gpu, grads_ref, tag=""):
+def check_grads(grads_gpu, grads_ref, tag="", rel=GRAD_REL):
     out = []
     for name, g, r in zip(("dQ", "dK", "dV"), grads_gpu, grads_ref):
         e = grad_rel(g, r)
-        assert e <= GRAD_REL, f"{tag} {name} relative-to-max error {e:.3e}"
+        assert e <= rel, f"{tag} {name} relative-to-max error {e:.3e}"
         out.append(e)
     return out

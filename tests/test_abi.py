@@ -31,7 +31,8 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     names = declared_symbols()
     for n in ("fa_fwd", "fa_fwd_kpad", "fa_bwd", "fa_bwd_workspace_bytes", "fa_blocksparse_fwd",
-              "fa_blocksparse_bwd", "fa_device_status", "fa_status_string", "fa_selftest_wait_timeout"):
+              "fa_blocksparse_bwd", "fa_dropout_fwd", "fa_dropout_bwd", "fa_dropout_mask",
+              "fa_device_status", "fa_status_string", "fa_selftest_wait_timeout"):
         assert n in names
 
 
@@ -151,3 +152,34 @@ def test_device_calls_fail_cleanly_without_gpu(L):
     # No device: status cannot be read, the self-test cannot launch.
     assert fa.device_status() in (fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
     assert L.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
+
+
+@needs_cpu
+@pytest.mark.parametrize("p,expect", [(1.0, 1), (-0.01, 1), (float("nan"), 1), (1.5, 1)])
+def test_dropout_rejects_invalid_probability(L, p, expect):
+    q, k, v, o, lse, do, dq, dk, dv, ws, keep = ptrs(11)
+    assert L.fa_dropout_fwd(q, k, v, o, lse, 1, 1, 128, 64, 0, 0.125, None, p, 1, 0, None) == expect
+    need = L.fa_bwd_workspace_bytes(1, 1, 128, 64)
+    assert L.fa_dropout_bwd(q, k, v, o, do, lse, dq, dk, dv, 1, 1, 128, 64, 0, 0.125, None, p, 1,
+                            0, ws, need, None) == expect
+    assert L.fa_dropout_mask(1, 1, 128, p, 1, 0, keep, None) == expect
+
+
+@needs_cpu
+def test_dropout_validates_like_the_plain_calls(L):
+    q, k, v, o, lse, keep = ptrs(6)
+    assert L.fa_dropout_fwd(q, k, v, o, lse, 1, 1, 128, 96, 0, 0.125, None, 0.1, 1, 0, None) == 2
+    assert L.fa_dropout_fwd(q, k, v, q, lse, 1, 1, 128, 64, 0, 0.125, None, 0.1, 1, 0, None) == 1
+    assert L.fa_dropout_mask(0, 1, 128, 0.1, 1, 0, keep, None) == 1
+    assert L.fa_dropout_mask(1, 1, 128, 0.1, 1, 0, None, None) == 1
+
+
+def test_python_dropout_arguments_checked_before_any_call():
+    import exact_io_aware_11_gb300 as fa
+    with pytest.raises(ValueError):
+        fa._lib._check_dropout(1.0, 0, 0)
+    with pytest.raises(ValueError):
+        fa._lib._check_dropout(0.1, -1, 0)
+    with pytest.raises(ValueError):
+        fa._lib._check_dropout(0.1, 0, 2 ** 32)
+    assert fa._lib._check_dropout(0.25, 2 ** 64 - 1, 2 ** 32 - 1) == (0.25, 2 ** 64 - 1, 2 ** 32 - 1)

@@ -44,6 +44,8 @@ class Workload:
     sparse: bool = False            # block-sparse forward (band + random blocks)
     sparse_band: int = 1            # |r - c| <= band is kept
     sparse_frac: float = 0.02       # fraction of off-band blocks kept
+    dropout: float = 0.0            # dropout probability on P (0: none)
+    dropout_seed: int = 0x5EED      # Philox key of the dropout draws
 
     @property
     def scale(self) -> float:
@@ -67,6 +69,9 @@ WORKLOADS = {
     # BERT-large shaped attention: 16 heads of 64, sequence 512, key padding.
     "bert_large": Workload("bert_large", 16, 16, 512, 64, causal=False, backward=True,
                            kv_len_range=(256, 512)),
+    # GPT-2 small with attention dropout 0.1, the rate GPT-2 trains with.
+    "gpt2_small_dropout": Workload("gpt2_small_dropout", 8, 12, 1024, 64, causal=True,
+                                   backward=True, dropout=0.1),
     # Block-sparse forward and backward at sequence 16K.
     "blocksparse": Workload("blocksparse", 2, 8, 16384, 64, causal=False, backward=True,
                             sparse=True),
@@ -75,6 +80,9 @@ for _n in (4096, 8192, 16384):
     for _c in (False, True):
         _w = _long(_n, _c)
         WORKLOADS[_w.name] = _w
+# Long context (N = 8192, d = 128, non-causal) with attention dropout 0.1.
+WORKLOADS["long_n8192_noncausal_dropout"] = _long(8192, False).with_(
+    name="long_n8192_noncausal_dropout", dropout=0.1)
 
 
 def block_mask_for(w: Workload, g: torch.Generator) -> torch.Tensor:
