@@ -155,14 +155,26 @@ class Step:
         self.fa, self.w = fa, w
         x = W.make_inputs(w, seed)
         self.host = x
-        self.q, self.k, self.v = (x[n].to(dev) for n in ("q", "k", "v"))
-        self.do = x["dout"].to(dev) if x["dout"] is not None else None
+        def place(t):  # [B, H, N, d] view of the workload's storage order
+            t = t.to(dev)
+            return t.transpose(1, 2).contiguous().transpose(1, 2) if w.layout == "bnhd" else t
+
+        self.q, self.k, self.v = (place(x[n]) for n in ("q", "k", "v"))
+        self.do = place(x["dout"]) if x["dout"] is not None else None
         self.kv = x["kv_len"].to(dev) if x["kv_len"] is not None else None
         self.mask = x["block_mask"].to(dev) if x["block_mask"] is not None else None
         B, H, N, d = w.B, w.H, w.N, w.d
-        self.o = torch.empty_like(self.q)
+        def like():
+            return torch.empty_strided(self.q.shape, self.q.stride(), dtype=self.q.dtype, device=dev)
+
+        self.o = like()
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.dq, self.dk, self.dv = (like() for _ in range(3))
+        self.opt = None
+        if w.layout != "bhnd":  # the general entry points take the strides
+            self.opt = fa.AttentionOptions()
+            self.opt.stride_b, self.opt.stride_h, self.opt.stride_n = self.q.stride()[:3]
+            self.opt.causal, self.opt.scale = int(w.causal), w.scale
         self.ws_bytes = fa.bwd_workspace_bytes(B, H, N, d)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.L = fa.lib()
@@ -170,7 +182,12 @@ class Step:
 
     def fwd(self, stream):
         w, L = self.w, self.L
-        if w.dropout > 0:
+        if self.opt is not None:
+            import ctypes
+            rc = L.fa_attention_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                    self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
+                                    ctypes.byref(self.opt), stream)
+        elif w.dropout > 0:
             rc = L.fa_dropout_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
                                   self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
                                   int(w.causal), w.scale,
@@ -189,6 +206,16 @@ class Step:
 
     def bwd_stages(self, stream):
         w, L = self.w, self.L
+        if self.opt is not None:  # one call runs all three kernels
+            import ctypes
+            yield L.fa_attention_bwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                     self.o.data_ptr(), self.do.data_ptr(), self.lse.data_ptr(),
+                                     self.dq.data_ptr(), self.dk.data_ptr(), self.dv.data_ptr(),
+                                     w.B, w.H, w.N, w.d, ctypes.byref(self.opt),
+                                     self.ws.data_ptr(), self.ws_bytes, stream)
+            yield 0
+            yield 0
+            return
         if w.dropout > 0:  # one call runs all three kernels
             yield L.fa_dropout_bwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
                                    self.o.data_ptr(), self.do.data_ptr(), self.lse.data_ptr(),
@@ -477,6 +504,8 @@ def sweep(fa, dev, flush, pk):
                 r["bwd_timing"] = "one fa_blocksparse_bwd call (preprocess, main, dQ convert)"
             elif w.dropout > 0:
                 r["bwd_timing"] = "one fa_dropout_bwd call (preprocess, main, dQ convert)"
+            elif w.layout != "bhnd":
+                r["bwd_timing"] = "one fa_attention_bwd call (preprocess, main, dQ convert)"
             else:
                 r["bwd_main_ms"] = round(statistics.median(t["bwd_main"]), 4)
         res[name] = r

@@ -47,6 +47,21 @@ SIGNATURES = {
 }
 
 
+class AttentionOptions(ctypes.Structure):
+    """fa_attention_options of include/fa.h."""
+    _fields_ = [("stride_b", ctypes.c_int64), ("stride_h", ctypes.c_int64),
+                ("stride_n", ctypes.c_int64), ("causal", ctypes.c_int), ("scale", ctypes.c_float),
+                ("kv_len", ctypes.c_void_p), ("block_mask", ctypes.c_void_p),
+                ("block_size", ctypes.c_int), ("dropout_p", ctypes.c_float),
+                ("dropout_seed", ctypes.c_uint64), ("dropout_offset", ctypes.c_uint32)]
+
+
+SIGNATURES["fa_attention_fwd"] = (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                       ctypes.POINTER(AttentionOptions), _P])
+SIGNATURES["fa_attention_bwd"] = (_I, [_P] * 9 + [_I, _I, _I, _I, ctypes.POINTER(AttentionOptions),
+                                                  _P, ctypes.c_size_t, _P])
+
+
 class FaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -251,6 +266,84 @@ def dropout_mask(B: int, H: int, N: int, dropout_p: float, seed: int, offset: in
     rc = lib().fa_dropout_mask(B, H, N, p, seed, offset, keep.data_ptr(), _stream_ptr(stream))
     _raise(rc, "fa_dropout_mask")
     return keep
+
+
+def _check_views(*ts):
+    """[B, H, N, d] bf16 CUDA views with a contiguous d axis and one set of strides."""
+    for t in ts:
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("exact attention runs on CUDA tensors only")
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError("expected bf16 [B, H, N, d] views with a contiguous last axis")
+        if t.shape != ts[0].shape or t.stride() != ts[0].stride():
+            raise ValueError("all [B, H, N, d] tensors of a call must share shape and strides")
+
+
+def _options(q, causal, scale, kv_len, block_mask, block_size, dropout_p, seed, offset):
+    B, H, N, d = q.shape
+    opt = AttentionOptions()
+    opt.stride_b, opt.stride_h, opt.stride_n = q.stride(0), q.stride(1), q.stride(2)
+    opt.causal = int(bool(causal))
+    opt.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if kv_len is not None and (kv_len.dtype != torch.int32 or not kv_len.is_cuda):
+        raise ValueError("kv_len must be a CUDA int32 tensor of shape [B]")
+    opt.kv_len = _ptr(kv_len)
+    if block_mask is not None:
+        if block_mask.dtype != torch.uint8 or not block_mask.is_cuda or not block_mask.is_contiguous():
+            raise ValueError("block_mask must be a contiguous CUDA uint8 tensor [nb, nb]")
+        nb = (N + block_size - 1) // block_size
+        if tuple(block_mask.shape) != (nb, nb):
+            raise ValueError(f"block_mask must have shape ({nb}, {nb})")
+    opt.block_mask = _ptr(block_mask)
+    opt.block_size = int(block_size)
+    p, seed, offset = _check_dropout(dropout_p, seed, offset)
+    opt.dropout_p, opt.dropout_seed, opt.dropout_offset = p, seed, offset
+    return opt
+
+
+def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, kv_len=None,
+                      block_mask=None, block_size: int = 128, dropout_p: float = 0.0,
+                      seed: int = 0, offset: int = 0, out=None, lse=None, stream=None):
+    """O, LSE with every option at once (fa_attention_fwd). q, k, v are
+    [B, H, N, d] views sharing one set of strides -- e.g. x.transpose(1, 2) of
+    a [B, N, H, d] tensor; O is returned with the same strides."""
+    _check_views(q, k, v)
+    B, H, N, d = q.shape
+    opt = _options(q, causal, scale, kv_len, block_mask, block_size, dropout_p, seed, offset)
+    o = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) if out is None else out
+    _check_views(q, o)
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    rc = lib().fa_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                l.data_ptr(), B, H, N, d, ctypes.byref(opt), _stream_ptr(stream))
+    _raise(rc, "fa_attention_fwd")
+    return o, l
+
+
+def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
+                       kv_len=None, block_mask=None, block_size: int = 128,
+                       dropout_p: float = 0.0, seed: int = 0, offset: int = 0, workspace=None,
+                       dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of attention_forward with the same options (fa_attention_bwd);
+    the gradients have the inputs' strides."""
+    _check_views(q, k, v, o, dout)
+    B, H, N, d = q.shape
+    opt = _options(q, causal, scale, kv_len, block_mask, block_size, dropout_p, seed, offset)
+    need = bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+
+    def like():
+        return torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+
+    dq = like() if dq is None else dq
+    dk = like() if dk is None else dk
+    dv = like() if dv is None else dv
+    _check_views(q, dq, dk, dv)
+    rc = lib().fa_attention_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                dv.data_ptr(), B, H, N, d, ctypes.byref(opt), ws.data_ptr(),
+                                ws.numel(), _stream_ptr(stream))
+    _raise(rc, "fa_attention_bwd")
+    return dq, dk, dv
 
 
 def device_status() -> int:

@@ -77,18 +77,87 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-// [B*H, N, d] bf16 as a 3-D tensor map; box = 64 columns (128 bytes) x 128 rows
-// x 1 head, 128-byte swizzle, zero fill outside the tensor (ragged N).
-bool encode_bhnd(CUtensorMap* map, const void* base, int B, int H, int N, int d) {
+// Validates the element strides (sb, sh, sn) of [B, H, N, d] tensors and
+// orders the row, head and batch axes by increasing stride for the tensor
+// maps. Requirements: strides >= 0 and multiples of 8 elements (16 bytes, the
+// tensor-map rule), below 2^36, and rows that do not overlap -- sorted by
+// stride, the smallest is >= d and each next one >= the previous stride times
+// its extent. An axis of extent 1 is placed last whatever its stride.
+bool make_strides(int B, int H, int N, int d, long long sb, long long sh, long long sn,
+                  Strides* out) {
+  const long long lim = 1LL << 36;
+  const long long st[3] = {sn, sh, sb};
+  const long long ext[3] = {N, H, B};
+  long long top = d;
+  for (int a = 0; a < 3; ++a) {
+    if (st[a] < 0 || st[a] >= lim || (st[a] & 7)) return false;
+    if (ext[a] > 1 && st[a] * ext[a] > top) top = st[a] * ext[a];
+  }
+  if (top >= lim) return false;
+  long long key[3];
+  int order[3] = {0, 1, 2};  // axes sorted by normalised stride (stable)
+  for (int a = 0; a < 3; ++a) key[a] = ext[a] > 1 ? st[a] : top;
+  for (int x = 0; x < 3; ++x)
+    for (int y = 0; y + 1 < 3 - x; ++y)
+      if (key[order[y]] > key[order[y + 1]]) {
+        const int t = order[y];
+        order[y] = order[y + 1];
+        order[y + 1] = t;
+      }
+  long long need = d;  // the smallest stride a row may have without overlap
+  for (int k = 0; k < 3; ++k) {
+    const int a = order[k];
+    if (ext[a] == 1) continue;
+    if (key[a] < need) return false;
+    need = key[a] * ext[a];
+  }
+  out->n = sn;
+  out->h = sh;
+  out->b = sb;
+  for (int k = 0; k < 3; ++k) {
+    if (order[k] == 0) out->pn = k;
+    if (order[k] == 1) out->ph = k;
+    if (order[k] == 2) out->pb = k;
+  }
+  return true;
+}
+
+// The row-major [B, H, N, d] strides (false if the tensor is too large).
+bool dense_strides(int B, int H, int N, int d, Strides* s) {
+  return make_strides(B, H, N, d, static_cast<long long>(H) * N * d, static_cast<long long>(N) * d,
+                      d, s);
+}
+
+// Bytes from the first to one past the last element of a tensor with strides s.
+size_t span_bytes(int B, int H, int N, int d, const Strides& s, size_t elem) {
+  return static_cast<size_t>((B - 1) * s.b + (H - 1) * s.h + (N - 1) * s.n + d) * elem;
+}
+
+// A bf16 [B, H, N, d] tensor with strides `st` as a 4-D tensor map: dimension
+// 0 is d, dimensions 1..3 the row, head and batch axes in the order st gives;
+// box = 64 columns (128 bytes) x 128 rows x 1 x 1, 128-byte swizzle, zero
+// fill outside the tensor (ragged N).
+bool encode_rows(CUtensorMap* map, const void* base, int B, int H, int N, int d,
+                 const Strides& st) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(B) * static_cast<cuuint64_t>(H)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlock), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  dims[0] = static_cast<cuuint64_t>(d);
+  box[0] = 64;
+  const long long ext[3] = {N, H, B};
+  const int pos[3] = {st.pn, st.ph, st.pb};
+  const long long sv[3] = {st.n, st.h, st.b};
+  long long top = d;  // the stride an axis of extent 1 is given (it is never stepped)
+  for (int a = 0; a < 3; ++a)
+    if (ext[a] > 1 && sv[a] * ext[a] > top) top = sv[a] * ext[a];
+  for (int a = 0; a < 3; ++a) {
+    dims[1 + pos[a]] = static_cast<cuuint64_t>(ext[a]);
+    strides[pos[a]] = static_cast<cuuint64_t>(ext[a] > 1 ? sv[a] : top) * 2;
+    box[1 + pos[a]] = a == 0 ? static_cast<cuuint32_t>(kBlock) : 1u;
+  }
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -141,15 +210,20 @@ size_t tensor_bytes(int B, int H, int N, int d, size_t elem) {
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int N, int d, int causal, float scale, const int32_t* kv_len,
                const uint8_t* block_mask, cudaStream_t stream,
-               const DropoutParams* drop = nullptr) {
+               const DropoutParams* drop = nullptr, const Strides* strides = nullptr) {
   int st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
+  Strides lay{};
+  if (strides)
+    lay = *strides;
+  else if (!dense_strides(B, H, N, d, &lay))
+    return FA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
   if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
-  const size_t tb = tensor_bytes(B, H, N, d, 2), lb = tensor_bytes(B, H, N, 1, 4);
+  const size_t tb = span_bytes(B, H, N, d, lay, 2), lb = tensor_bytes(B, H, N, 1, 4);
   const void* ins[3] = {q, k, v};
   for (const void* in : ins)
     if (overlaps(o, tb, in, tb) || overlaps(lse, lb, in, tb)) return FA_ERR_INVALID_ARG;
@@ -159,9 +233,10 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if (st != FA_OK) return st;
   FwdLaunch a;
   std::memset(&a, 0, sizeof(a));
-  if (!encode_bhnd(&a.tm_q, q, B, H, N, d) || !encode_bhnd(&a.tm_k, k, B, H, N, d) ||
-      !encode_bhnd(&a.tm_v, v, B, H, N, d) || !encode_bhnd(&a.tm_o, o, B, H, N, d))
+  if (!encode_rows(&a.tm_q, q, B, H, N, d, lay) || !encode_rows(&a.tm_k, k, B, H, N, d, lay) ||
+      !encode_rows(&a.tm_v, v, B, H, N, d, lay))
     return FA_ERR_CUDA;
+  a.st = lay;
   a.o = o;
   a.lse = lse;
   a.B = B;
@@ -195,9 +270,15 @@ struct BwdPtrs {
 // not use may be NULL; every pointer a stage uses must be non-NULL.
 int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int causal, float scale,
                const int32_t* kv_len, size_t workspace_bytes, cudaStream_t stream,
-               const uint8_t* block_mask = nullptr, const DropoutParams* drop = nullptr) {
+               const uint8_t* block_mask = nullptr, const DropoutParams* drop = nullptr,
+               const Strides* strides = nullptr) {
   int st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
+  Strides lay{};
+  if (strides)
+    lay = *strides;
+  else if (!dense_strides(B, H, N, d, &lay))
+    return FA_ERR_INVALID_ARG;
   const bool pre = stages & kBwdStagePre, mainst = stages & kBwdStageMain,
              conv = stages & kBwdStageConvert;
   if (!p.ws) return FA_ERR_INVALID_ARG;
@@ -211,7 +292,7 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
   if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
   const BwdWorkspace ws = bwd_workspace_layout(B, H, N, d);
   if (workspace_bytes < ws.total) return FA_ERR_INVALID_ARG;
-  const size_t tb = tensor_bytes(B, H, N, d, 2), lb = tensor_bytes(B, H, N, 1, 4);
+  const size_t tb = span_bytes(B, H, N, d, lay, 2), lb = tensor_bytes(B, H, N, 1, 4);
   const void* ins[] = {p.q, p.k, p.v, p.o, p.dout};
   void* outs[] = {p.dq, p.dk, p.dv};
   for (int x = 0; x < 3; ++x) {
@@ -234,11 +315,13 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
   std::memset(&a, 0, sizeof(a));
   uint8_t* wsb = static_cast<uint8_t*>(p.ws);
   const int npad = (N + kBlock - 1) / kBlock * kBlock;
-  if (mainst && (!encode_bhnd(&a.tm_q, p.q, B, H, N, d) || !encode_bhnd(&a.tm_k, p.k, B, H, N, d) ||
-                 !encode_bhnd(&a.tm_v, p.v, B, H, N, d) ||
-                 !encode_bhnd(&a.tm_do, p.dout, B, H, N, d) ||
+  if (mainst && (!encode_rows(&a.tm_q, p.q, B, H, N, d, lay) ||
+                 !encode_rows(&a.tm_k, p.k, B, H, N, d, lay) ||
+                 !encode_rows(&a.tm_v, p.v, B, H, N, d, lay) ||
+                 !encode_rows(&a.tm_do, p.dout, B, H, N, d, lay) ||
                  !encode_f32_rows(&a.tm_dqacc, wsb + ws.dq_off, B * H, npad, d)))
     return FA_ERR_CUDA;
+  a.st = lay;
   a.o = p.o;
   a.dout = p.dout;
   a.lse = p.lse;
@@ -367,6 +450,53 @@ int fa_dropout_mask(int B, int H, int N, float dropout_p, uint64_t seed, uint32_
   const int st = current_device_info(&dev);
   if (st != FA_OK) return st;
   return launch_dropout_mask(drop, B * H, N, keep, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+namespace {
+
+// Strides, dropout and the remaining checks of fa_attention_fwd / _bwd.
+int attention_options(const fa_attention_options* opt, int B, int H, int N, int d, Strides* lay,
+                      DropoutParams* drop, bool* use_drop) {
+  if (opt == nullptr || B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (opt->stride_b == 0 && opt->stride_h == 0 && opt->stride_n == 0) {
+    if (!dense_strides(B, H, N, d, lay)) return FA_ERR_INVALID_ARG;
+  } else if (!make_strides(B, H, N, d, opt->stride_b, opt->stride_h, opt->stride_n, lay)) {
+    return FA_ERR_INVALID_ARG;
+  }
+  if (opt->block_mask != nullptr && opt->block_size != kBlock) return FA_ERR_UNSUPPORTED;
+  *use_drop = opt->dropout_p != 0.f;
+  if (*use_drop && !make_dropout(opt->dropout_p, opt->dropout_seed, opt->dropout_offset, drop))
+    return FA_ERR_INVALID_ARG;  // negative, NaN or >= 1
+  return FA_OK;
+}
+
+}  // namespace
+
+int fa_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, const fa_attention_options* opt,
+                     struct CUstream_st* stream) {
+  Strides lay{};
+  DropoutParams drop{};
+  bool use_drop = false;
+  const int st = attention_options(opt, B, H, N, d, &lay, &drop, &use_drop);
+  if (st != FA_OK) return st;
+  return fwd_common(q, k, v, o, lse, B, H, N, d, opt->causal, opt->scale, opt->kv_len,
+                    opt->block_mask, stream, use_drop ? &drop : nullptr, &lay);
+}
+
+int fa_attention_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                     int H, int N, int d, const fa_attention_options* opt, void* workspace,
+                     size_t workspace_bytes, struct CUstream_st* stream) {
+  Strides lay{};
+  DropoutParams drop{};
+  bool use_drop = false;
+  const int st = attention_options(opt, B, H, N, d, &lay, &drop, &use_drop);
+  if (st != FA_OK) return st;
+  const BwdPtrs p{q, k, v, o, dout, lse, dq, dk, dv, workspace};
+  return bwd_common(kBwdStageAll, p, B, H, N, d, opt->causal, opt->scale, opt->kv_len,
+                    workspace_bytes, stream, opt->block_mask, use_drop ? &drop : nullptr, &lay);
 }
 
 int fa_bwd_preprocess(const void* o, const void* dout, const float* lse, int B, int H, int N,

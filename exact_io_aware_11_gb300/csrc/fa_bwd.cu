@@ -1,7 +1,8 @@
 // Backward pass of exact attention: the preprocess and dQ-conversion stages,
-// the dense, causal, key-padded and block-sparse variants of the main kernel
-// (fa_bwd_kernel.cuh; the dropout variants are compiled in fa_bwd_dropout.cu)
-// and the watchdog self-test kernel.
+// the dense (causal or not, key-padded or not) variants of the main kernel
+// (fa_bwd_kernel.cuh) and the watchdog self-test kernel. The block-sparse and
+// dropout variants of the main kernel are compiled in fa_bwd_sparse.cu,
+// fa_bwd_dropout.cu and fa_bwd_dropout_sparse.cu.
 #include "fa_bwd_kernel.cuh"
 
 namespace fa {
@@ -36,21 +37,21 @@ cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
   if (stages & kBwdStagePre) {
     e = launch_pdl(bwd_pre_kernel<D>, dim3(grid_for(static_cast<long long>(BH) * Npad * (D / 8))),
                    dim3(256), 0, stream, a.o, a.dout, a.lse, a.lse2, a.delta, a.dq_acc, BH, a.N,
-                   Npad);
+                   Npad, a.st, a.H);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageMain) {
     if (a.drop.enabled)
       e = launch_bwd_main_dropout(a, stream);
-    else if (!CAUSAL && a.block_mask != nullptr)
-      e = launch_bwd_main_t<D, false, true, false>(a, stream);
+    else if (a.block_mask != nullptr)
+      e = launch_bwd_main_sparse(a, stream);
     else
       e = launch_bwd_main_t<D, CAUSAL, false, false>(a, stream);
     if (e != cudaSuccess) return e;
   }
   if (stages & kBwdStageConvert) {
     e = launch_pdl(dq_convert_kernel<D>, dim3(grid_for(static_cast<long long>(BH) * a.N * (D / 8))),
-                   dim3(256), 0, stream, a.dq_acc, a.dq, BH, a.N, Npad);
+                   dim3(256), 0, stream, a.dq_acc, a.dq, BH, a.N, Npad, a.st, a.H);
   }
   return e;
 }

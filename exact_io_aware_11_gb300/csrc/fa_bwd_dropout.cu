@@ -9,6 +9,7 @@
 namespace fa {
 
 cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, cudaStream_t stream) {
+  if (a.block_mask != nullptr) return launch_bwd_main_dropout_sparse(a, stream);
   const bool causal = a.causal != 0;
   if (a.d == 64)
     return causal ? launch_bwd_main_t<64, true, false, true>(a, stream)

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       float* __restrict__ lse2,
                                                       float* __restrict__ delta,
                                                       float* __restrict__ dq_acc, int BH, int N,
-                                                      int Npad) {
+                                                      int Npad, Strides st, int H) {
   constexpr int kPer = D / 8;  // threads per row (8 elements = 16 bytes each)
   grid_dep_wait();
   grid_dep_launch();
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const bool valid = in && n < N;
     float acc = 0.f;
     if (valid) {
-      const size_t off = (static_cast<size_t>(bh) * N + n) * D + part * 8;
+      const long long off = row_offset(st, H, bh, n) + part * 8;
       const uint4 a = *reinterpret_cast<const uint4*>(o + off);
       const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
       const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 template <int D>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ dq_acc,
                                                          __nv_bfloat16* __restrict__ dq, int BH,
-                                                         int N, int Npad) {
+                                                         int N, int Npad, Strides st, int H) {
   constexpr int kPer = D / 8;
   grid_dep_wait();
   grid_dep_launch();
@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
     w.y = pack_bf16(a.z, a.w);
     w.z = pack_bf16(b.x, b.y);
     w.w = pack_bf16(b.z, b.w);
-    *reinterpret_cast<uint4*>(dq + row * D + part * 8) = w;
+    *reinterpret_cast<uint4*>(dq + row_offset(st, H, static_cast<int>(bh), static_cast<int>(n)) +
+                              part * 8) = w;
   }
 }
 
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 // dK and dV rows are written as zeros.
 struct BwdGrid {
   int H, N, nt, BH, n_items;
+  Strides st;  // of q, k, v, dout, dk, dv
   const int32_t* kv_len;
   const uint8_t* mask;  // block-sparse: uint8 [nt][nt], nonzero = (query tile, key tile) kept
 };
@@ -216,11 +218,11 @@ __device__ __forceinline__ BwdItem make_bwd_item(const BwdGrid& g, int k) {
   if (g.kv_len != nullptr) x.kv_bound = min(g.N, max(0, g.kv_len[x.bh / g.H]));
   x.i0 = CAUSAL ? x.j : 0;
   x.n_iter = x.j * kBlock < x.kv_bound ? g.nt - x.i0 : 0;
-  if constexpr (SPARSE) {  // the query tiles whose mask row keeps key tile j
+  if constexpr (SPARSE) {  // the query tiles (i >= j if causal) whose mask row keeps key tile j
     int n = 0;
-    for (int i = 0; i < g.nt; ++i) n += g.mask[static_cast<size_t>(i) * g.nt + x.j] != 0;
-    x.n_iter = n;
-    x.i0 = bwd_next_row<true>(g, x.j, 0);
+    for (int i = x.i0; i < g.nt; ++i) n += g.mask[static_cast<size_t>(i) * g.nt + x.j] != 0;
+    x.n_iter = x.j * kBlock < x.kv_bound ? n : 0;
+    x.i0 = bwd_next_row<true>(g, x.j, x.i0);
   }
   return x;
 }
@@ -282,7 +284,7 @@ struct BwdCursor {
 // the compute warps already form P of the next item.
 // DROP: dropout (fa_philox.cuh) regenerated from the element indices: dV is
 // accumulated from the dropped P^T (its 1 / (1 - p') applied when dV leaves
-// TMEM) and dS = P * (Z dP_dropped / (1 - p') - D). Dense (SPARSE = false) only.
+// TMEM) and dS = P * (Z dP_dropped / (1 - p') - D).
 template <int D, bool CAUSAL, bool SPARSE, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -291,7 +293,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __nv_bfloat16* __restrict__ dv, const float* __restrict__ lse2,
                     const float* __restrict__ delta, BwdGrid grid, int Npad, float scale,
                     DropoutParams dp, int* status, long long wait_limit) {
-  static_assert(!(DROP && SPARSE), "dropout is compiled for the dense kernel only");
   using L = BwdLayout<D>;
   constexpr int QS = L::kQS, DS = L::kDS, KVS = L::kKVS;
   extern __shared__ uint8_t smem_raw[];
@@ -387,8 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar_kvfull + kvs, 2 * L::kTile);
         uint8_t* kv = smem + L::kKV + kvs * 2 * L::kTile;
         for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_3d(kv + c * kChunk, &tm_k, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh);
-          tma_load_3d(kv + L::kTile + c * kChunk, &tm_v, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh);
+          tma_load_rows(kv + c * kChunk, &tm_k, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh % grid.H,
+                        x.bh / grid.H, grid.st);
+          tma_load_rows(kv + L::kTile + c * kChunk, &tm_v, bar_kvfull + kvs, c * 64, x.j * kBlock,
+                        x.bh % grid.H, x.bh / grid.H, grid.st);
         }
         ++t;
         for (int it = 0, i = x.i0; it < x.n_iter; ++it, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
@@ -396,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (gq >= QS && !mbar_wait(bar_qempty + qs, ((gq / QS) - 1) & 1, wd)) { ok = false; break; }
           mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
-                        i * kBlock, x.bh);
+            tma_load_rows(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
+                        i * kBlock, x.bh % grid.H, x.bh / grid.H, grid.st);
           const size_t roff = static_cast<size_t>(x.bh) * Npad + static_cast<size_t>(i) * kBlock;
           bulk_load(smem + L::kStat + qs * 1024, lse2 + roff, 512, bar_qfull + qs);
           bulk_load(smem + L::kStat + qs * 1024 + 512, delta + roff, 512, bar_qfull + qs);
@@ -405,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (gq >= DS && !mbar_wait(bar_doempty + ds, ((gq / DS) - 1) & 1, wd)) { ok = false; break; }
           mbar_expect_tx(bar_dofull + ds, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
-                        i * kBlock, x.bh);
+            tma_load_rows(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
+                        i * kBlock, x.bh % grid.H, x.bh / grid.H, grid.st);
           do_issued = gq + 1;
         }
       }
@@ -552,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k < 0) break;
       const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
       const int key = x.j * kBlock + row;
-      const size_t out_off = (static_cast<size_t>(x.bh) * N + key) * D;
+      const long long out_off = row_offset(grid.st, grid.H, x.bh, key);
       if (x.n_iter == 0) {  // no valid key in this tile: zero gradients
         if (key < N) {
           uint4* a = reinterpret_cast<uint4*>(dk + out_off);
@@ -657,9 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (k < 0) break;
       const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
       const bool key_live = x.j * kBlock + kr < x.kv_bound;
-      for (int it = 0; it < x.n_iter; ++it, ++gq) {
-        const int s = gq % QS;
-        const int i = x.i0 + it;  // Q tile (dense): the causal diagonal and the dropout draws
+      for (int it = 0, i = x.i0; it < x.n_iter; ++it, ++gq, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
+        const int s = gq % QS;  // i: the Q tile (causal diagonal, dropout draws)
         const float* st_lse = reinterpret_cast<const float*>(smem + L::kStat + s * 1024) + qc0;
         const float* st_delta = st_lse + 128;
         if (!mbar_wait_warp(bar_qfull + s, (gq / QS) & 1, wd)) { ok = false; break; }
@@ -794,6 +796,7 @@ cudaError_t launch_bwd_main_t(const BwdLaunch& a, cudaStream_t stream) {
   g.n_items = BH * nt;
   g.kv_len = a.kv_len;
   g.mask = a.block_mask;
+  g.st = a.st;
   return launch_pdl(kern, dim3(min(g.n_items, sm_count())), dim3(kThreads), L::kSmem, stream,
                     a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g,
                     nt * kBlock, a.scale, a.drop, a.status, a.wait_limit);

@@ -138,6 +138,7 @@ struct FwdItem {
 
 struct FwdGrid {
   int H, N, nqt, npairs, n_items;
+  Strides st;  // of q, k, v, o
   const int32_t* kv_len;
   const uint8_t* block_mask;
 };
@@ -271,8 +272,8 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           if (nq >= QS && !mbar_wait(bar_qempty + qb, ((nq / QS) - 1) & 1, wd)) { ok = false; break; }
           mbar_expect_tx(bar_qfull + qb, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kQ + qb * L::kTile + c * kChunk, &tm_q, bar_qfull + qb, c * 64,
-                        (t ? it.qtB : it.qtA) * kBlock, it.bh);
+            tma_load_rows(smem + L::kQ + qb * L::kTile + c * kChunk, &tm_q, bar_qfull + qb, c * 64,
+                        (t ? it.qtB : it.qtA) * kBlock, it.bh % g.H, it.bh / g.H, g.st);
           ++nq;
         }
         for (int j = 0; ok && j < it.uend; ++j) {
@@ -281,14 +282,14 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           if (u >= KS && !mbar_wait(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) { ok = false; break; }
           mbar_expect_tx(bar_kfull + ks, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
-                        j * kBlock, it.bh);
+            tma_load_rows(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
+                        j * kBlock, it.bh % g.H, it.bh / g.H, g.st);
           k_issued = u + 1;
           if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) { ok = false; break; }
           mbar_expect_tx(bar_vfull + vs, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
-                        j * kBlock, it.bh);
+            tma_load_rows(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
+                        j * kBlock, it.bh % g.H, it.bh / g.H, g.st);
           v_issued = u + 1;
           ++u;
         }
@@ -701,7 +702,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       const bool live = have && l > 0.f;
       const float inv = live ? (DROP ? dp.rescale : 1.f) / l : 0.f;
       const bool row_ok = row < g.N;
-      uint4* orow = reinterpret_cast<uint4*>(out + (static_cast<size_t>(it.bh) * g.N + row) * D);
+      uint4* orow = reinterpret_cast<uint4*>(out + row_offset(g.st, g.H, it.bh, row));
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
         uint32_t o[32];
@@ -752,6 +753,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
   g.n_items = a.B * a.H * g.npairs;
   g.kv_len = a.kv_len;
   g.block_mask = a.block_mask;
+  g.st = a.st;
   const int grid = min(g.n_items, sm_count());
   const float scale_log2 = a.scale * 1.4426950408889634f;
   return launch_pdl(kern, dim3(grid), dim3(FwdWarps<D>::kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,

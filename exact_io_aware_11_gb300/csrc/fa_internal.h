@@ -15,6 +15,31 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 // Rows of one Q tile and one K/V tile (the 128 x 128 block of the method).
 constexpr int kBlock = 128;
 
+// Element strides of the [B, H, N, d] tensors of one call (q, k, v, o, dout,
+// dq, dk, dv share them): element (b, h, n, c) sits at b*b + h*h + n*n + c.
+// [B, H, N, d] row-major is {H*N*d, N*d, d}; [B, N, H, d] is {N*H*d, d, H*d}.
+// The tensor maps over these tensors are 4-D: d, then the row, head and batch
+// axes in order of increasing stride; pn, ph, pb give the positions (0..2
+// among dimensions 1..3) of the row, head and batch coordinates.
+struct Strides {
+  long long b, h, n;
+  int pn, ph, pb;
+};
+
+// Coordinates (dimensions 1..3) of row n of head h in batch b.
+__device__ __forceinline__ void row_coords(const Strides& s, int n, int h, int b, int& y0, int& y1,
+                                           int& y2) {
+  y0 = s.pn == 0 ? n : (s.ph == 0 ? h : b);
+  y1 = s.pn == 1 ? n : (s.ph == 1 ? h : b);
+  y2 = s.pn == 2 ? n : (s.ph == 2 ? h : b);
+}
+
+// Offset in elements of row n of problem bh = b*H + h.
+__host__ __device__ __forceinline__ long long row_offset(const Strides& s, int H, int bh, int n) {
+  return static_cast<long long>(bh / H) * s.b + static_cast<long long>(bh % H) * s.h +
+         static_cast<long long>(n) * s.n;
+}
+
 // Dropout on the attention probabilities (inverted: kept entries are scaled
 // by 1 / (1 - p')). Element (b, h, i, j) draws byte j mod 16 of the
 // Philox4x32-10 block at counter (j / 16, i, b*H + h, offset) under key
@@ -28,10 +53,11 @@ struct DropoutParams {
 };
 
 struct FwdLaunch {
-  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H, N, d], box 64 x 128 x 1, 128B swizzle
+  CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps (d, N, H, B) with the call's strides, box 64 x 128 x 1 x 1, 128B swizzle
   void* o;
   float* lse;
   int B, H, N, d;
+  Strides st;
   int causal;
   float scale;
   const int32_t* kv_len;      // device [B] or nullptr
@@ -42,7 +68,7 @@ struct FwdLaunch {
 };
 
 struct BwdLaunch {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as above
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as above (4-D, the call's strides)
   CUtensorMap tm_dqacc;  // fp32 [B*H, Npad, d] accumulator, box 32 x 128 x 1, 128B swizzle
   const void* o;
   const void* dout;
@@ -51,6 +77,7 @@ struct BwdLaunch {
   void* dk;
   void* dv;
   int B, H, N, d;
+  Strides st;
   int causal;
   float scale;
   const int32_t* kv_len;
@@ -95,10 +122,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
-// The dropout variants (a.drop.enabled != 0), compiled in their own
-// translation units: the forward kernel and the backward main kernel.
+// Variants compiled in their own translation units: the forward kernel with
+// dropout (a.drop.enabled != 0); the backward main kernel with a block mask,
+// with dropout, and with both.
 cudaError_t launch_fwd_dropout(const FwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd_main_sparse(const BwdLaunch& a, cudaStream_t stream);
 cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, cudaStream_t stream);
+cudaError_t launch_bwd_main_dropout_sparse(const BwdLaunch& a, cudaStream_t stream);
 // Writes the keep decisions Z (1 = kept) of a.drop for [B*H, N, N] as bytes.
 cudaError_t launch_dropout_mask(const DropoutParams& drop, int BH, int N, uint8_t* keep,
                                 cudaStream_t stream);

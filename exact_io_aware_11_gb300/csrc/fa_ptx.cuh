@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 
 #include "fa.h"
+#include "fa_internal.h"
 
 namespace fa {
 
@@ -196,6 +197,25 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 4-D tiled load (x = innermost, in elements) into shared memory.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// 128 rows (starting at `row`) x 64 columns (starting at `x`) of head h,
+// batch b from a 4-D [B, H, N, d] map whose outer dimensions follow `st`.
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int x, int row, int h, int b, const Strides& st) {
+  int y0, y1, y2;
+  row_coords(st, row, h, b, y0, y1, y2);
+  tma_load_4d(dst, map, bar, x, y0, y1, y2);
 }
 
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).

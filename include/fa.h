@@ -207,6 +207,52 @@ int fa_dropout_bwd(const void* q, const void* k, const void* v, const void* o, c
 int fa_dropout_mask(int B, int H, int N, float dropout_p, uint64_t seed, uint32_t offset,
                     uint8_t* keep, struct CUstream_st* stream);
 
+/* Options of fa_attention_fwd / fa_attention_bwd, the general entry points:
+ * every combination of layout, causal mask, key padding, block mask and
+ * dropout in one call. Zero-initialise, then set scale and what is needed.
+ *   stride_b, stride_h, stride_n : element strides of the batch, head and row
+ *       axes, shared by every bf16 [B, H, N, d] tensor of the call (q, k, v,
+ *       o; dout, dq, dk, dv); the d axis is contiguous. All three 0 means
+ *       row-major [B, H, N, d]. [B, N, H, d] storage is {N*H*d, d, H*d}.
+ *       Each must be >= 0, a multiple of 8 (16 bytes) and < 2^36, and rows
+ *       must not overlap: sorted by stride (axes of extent 1 excluded), the
+ *       smallest is >= d and each next is >= the previous stride times that
+ *       axis' extent. lse stays fp32 [B, H, N] row-major.
+ *   causal       : 0 or 1 (keeps j <= i).
+ *   scale        : finite, > 0.
+ *   kv_len       : DEVICE int32 [B] or NULL (as fa_fwd_kpad).
+ *   block_mask, block_size : as fa_blocksparse_fwd, or NULL / ignored. With
+ *       causal = 1 a block is visited only if kept and not above the diagonal.
+ *   dropout_p, dropout_seed, dropout_offset : as fa_dropout_fwd; dropout_p = 0
+ *       means no dropout.
+ * Every mask applies together (an element is kept if it passes all of them). */
+typedef struct fa_attention_options {
+  int64_t stride_b, stride_h, stride_n;
+  int causal;
+  float scale;
+  const int32_t* kv_len;
+  const uint8_t* block_mask;
+  int block_size;
+  float dropout_p;
+  uint64_t dropout_seed;
+  uint32_t dropout_offset;
+} fa_attention_options;
+
+/* Forward pass with options: O and LSE as fa_fwd / fa_fwd_kpad /
+ * fa_blocksparse_fwd / fa_dropout_fwd, which are this call with the
+ * corresponding options. Errors as those calls, plus FA_ERR_INVALID_ARG for a
+ * NULL opt or strides that break the rules above. */
+int fa_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, const fa_attention_options* opt,
+                     struct CUstream_st* stream);
+
+/* Backward pass of fa_attention_fwd with the same options (o and lse from
+ * that call): dq, dk, dv in the same strides. Workspace and errors as fa_bwd. */
+int fa_attention_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                     int H, int N, int d, const fa_attention_options* opt, void* workspace,
+                     size_t workspace_bytes, struct CUstream_st* stream);
+
 /* Device-side status of the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT
  * if a bounded wait inside a kernel gave up since the last call. Reading
  * clears it. Call only after synchronising the streams that ran the

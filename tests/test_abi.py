@@ -183,3 +183,43 @@ def test_python_dropout_arguments_checked_before_any_call():
     with pytest.raises(ValueError):
         fa._lib._check_dropout(0.1, 0, 2 ** 32)
     assert fa._lib._check_dropout(0.25, 2 ** 64 - 1, 2 ** 32 - 1) == (0.25, 2 ** 64 - 1, 2 ** 32 - 1)
+
+
+def _opts(**kw):
+    from exact_io_aware_11_gb300 import AttentionOptions
+    o = AttentionOptions()
+    o.scale = 0.125
+    o.block_size = 128
+    for k_, v_ in kw.items():
+        setattr(o, k_, v_)
+    return o
+
+
+@needs_cpu
+@pytest.mark.parametrize("strides,expect", [
+    ((0, 0, 0), 3),                                   # row-major [B,H,N,d]: valid (no device here)
+    ((256 * 4 * 64, 64, 4 * 64), 3),                  # [B,N,H,d]
+    ((4 * 256 * 128, 256 * 128, 128), 3),             # rows padded to 128 elements
+    ((4 * 256 * 64, 256 * 64, 68), 1),                # row stride not a multiple of 8
+    ((4 * 256 * 64, 256 * 64 - 8, 64), 1),            # heads overlap
+    ((4 * 256 * 64, 64, 64), 1),                      # rows of different heads overlap
+    ((-4 * 256 * 64, 256 * 64, 64), 1),               # negative
+    ((4 * 256 * 64, 256 * 64, 56), 1),                # row stride < d
+])
+def test_attention_strides_validated(L, strides, expect):
+    import ctypes
+    q, k, v, o, lse = ptrs(5)
+    opt = _opts(stride_b=strides[0], stride_h=strides[1], stride_n=strides[2])
+    assert L.fa_attention_fwd(q, k, v, o, lse, 2, 4, 256, 64, ctypes.byref(opt), None) == expect
+
+
+@needs_cpu
+def test_attention_options_validated(L):
+    import ctypes
+    q, k, v, o, lse, m = ptrs(6)
+    assert L.fa_attention_fwd(q, k, v, o, lse, 1, 1, 128, 64, None, None) == 1
+    for kw, expect in [(dict(dropout_p=1.0), 1), (dict(dropout_p=-0.5), 1), (dict(causal=3), 1),
+                       (dict(scale=0.0), 1), (dict(block_mask=m, block_size=64), 2),
+                       (dict(block_mask=m, causal=1, dropout_p=0.3), 3)]:
+        opt = _opts(**kw)
+        assert L.fa_attention_fwd(q, k, v, o, lse, 1, 1, 128, 64, ctypes.byref(opt), None) == expect, kw

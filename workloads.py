@@ -46,6 +46,7 @@ class Workload:
     sparse_frac: float = 0.02       # fraction of off-band blocks kept
     dropout: float = 0.0            # dropout probability on P (0: none)
     dropout_seed: int = 0x5EED      # Philox key of the dropout draws
+    layout: str = "bhnd"            # storage order of Q, K, V, dO, O, dQ, dK, dV: bhnd or bnhd
 
     @property
     def scale(self) -> float:
@@ -72,6 +73,9 @@ WORKLOADS = {
     # GPT-2 small with attention dropout 0.1, the rate GPT-2 trains with.
     "gpt2_small_dropout": Workload("gpt2_small_dropout", 8, 12, 1024, 64, causal=True,
                                    backward=True, dropout=0.1),
+    # GPT-2 small with Q, K, V, O and gradients stored as [B, N, H, d].
+    "gpt2_small_bnhd": Workload("gpt2_small_bnhd", 8, 12, 1024, 64, causal=True, backward=True,
+                                layout="bnhd"),
     # Block-sparse forward and backward at sequence 16K.
     "blocksparse": Workload("blocksparse", 2, 8, 16384, 64, causal=False, backward=True,
                             sparse=True),
