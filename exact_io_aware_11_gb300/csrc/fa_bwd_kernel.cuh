@@ -112,6 +112,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   grid_dep_launch();
   const long long total = static_cast<long long>(BH) * Npad * kPer;
   const long long total32 = (total + 31) & ~31LL;
+  // Row-major [B, H, N, d] (the common case) needs no division by H.
+  const bool dense = st.n == D && st.h == static_cast<long long>(N) * D &&
+                     st.b == static_cast<long long>(H) * N * D;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total32;
        g += stride) {
@@ -123,7 +126,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const bool valid = in && n < N;
     float acc = 0.f;
     if (valid) {
-      const long long off = row_offset(st, H, bh, n) + part * 8;
+      const long long off = (dense ? (static_cast<long long>(bh) * N + n) * D
+                                   : row_offset(st, H, bh, n)) + part * 8;
       const uint4 a = *reinterpret_cast<const uint4*>(o + off);
       const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
       const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -165,6 +169,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   grid_dep_launch();
   const long long total = static_cast<long long>(BH) * N * kPer;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const bool dense = st.n == D && st.h == static_cast<long long>(N) * D &&
+                     st.b == static_cast<long long>(H) * N * D;
   for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
        g += stride) {
     const long long row = g / kPer;  // over [BH, N]
@@ -178,8 +184,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
     w.y = pack_bf16(a.z, a.w);
     w.z = pack_bf16(b.x, b.y);
     w.w = pack_bf16(b.z, b.w);
-    *reinterpret_cast<uint4*>(dq + row_offset(st, H, static_cast<int>(bh), static_cast<int>(n)) +
-                              part * 8) = w;
+    const long long off = dense ? row * D : row_offset(st, H, static_cast<int>(bh), static_cast<int>(n));
+    *reinterpret_cast<uint4*>(dq + off + part * 8) = w;
   }
 }
 

@@ -107,7 +107,9 @@ def test_causal_block_sparse(fa, d, N):
 @pytest.mark.parametrize("causal", [False, True])
 def test_every_option_at_once(fa, d, causal):
     # [B, N, H, d] storage + key padding + block mask + dropout (+ causal).
-    kv = torch.tensor([1, 300, 777], dtype=torch.int32)
+    # Rows that see exactly one key are left to the next test: there the
+    # exact softmax gradient is zero and what remains is the rounding of D.
+    kv = torch.tensor([2, 300, 777], dtype=torch.int32)
     w, x = generic(3, 2, 777, d, causal, seed=50 + d)
     nb = 7
     m = _random_mask(nb, d + int(causal), empty_row=4)
@@ -128,3 +130,36 @@ def test_every_option_at_once(fa, d, causal):
     ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, causal=causal,
                           kv_len=kv.numpy(), block_mask=m, dropout=drop)
     check_grads(g, ref, f"all options d={d} causal={causal}", GRAD_REL * r)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_visible_key_with_dropout(fa, d):
+    # Batch 0 sees only key 0 (kv_len = 1), so P = 1 there, O_i = Z_i0 r v_0,
+    # and the exact dS of every row is 0: dQ = 0 for the batch and dK is 0
+    # except that the kernel forms D = rowsum(dO * O) from the bf16 O, so each
+    # kept row adds dO_i . (r v_0 - bf16(r v_0)) to dS_i0. That is bounded by
+    # |delta D_i| <= sum_c |dO_ic| * 2^-8 |O_ic| (bf16 half-ulp), which gives
+    # |dK_0| <= scale * sum_i |delta D_i| |q_i| per column (plus fp32 and the
+    # bf16 rounding of dS and dK). The other batch is checked against the oracle.
+    kv = torch.tensor([1, 400], dtype=torch.int32)
+    w, x = generic(2, 2, 400, d, False, seed=60 + d)
+    p, seed, off = 0.2, 77, 0
+    q, k, v, do = cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["dout"])
+    kw = dict(kv_len=kv.cuda(), dropout_p=p, seed=seed, offset=off)
+    o, lse = fa.attention_forward(q, k, v, **kw)
+    dq, dk, dv = fa.attention_backward(q, k, v, o, do, lse, **kw)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    assert torch.count_nonzero(dk[0, :, 1:]) == 0 and torch.count_nonzero(dv[0, :, 1:]) == 0
+    qq, kk, oo, dd = f64(q[0]), f64(k[0]), f64(o[0]), f64(do[0])
+    delta = (np.abs(dd) * np.abs(oo) * 2.0 ** -8).sum(-1)              # [H, N] bound on |delta D|
+    bound_k = w.scale * (delta[..., None] * np.abs(qq)).sum(1)         # [H, d]: |dK_0|
+    bound_q = w.scale * delta[..., None] * np.abs(kk[:, :1, :])        # [H, N, d]: |dQ_i|
+    got_k, got_q = np.abs(f64(dk[0, :, 0])), np.abs(f64(dq[0]))
+    assert np.all(got_k <= 1.02 * bound_k + 1e-3), (got_k / (bound_k + 1e-9)).max()
+    assert np.all(got_q <= 1.02 * bound_q + 1e-3), (got_q / (bound_q + 1e-9)).max()
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, kv_len=kv.numpy(),
+                          heads=[(1, 0), (1, 1)], dropout=(float(np.float32(p)), seed, off))
+    r = oracle.rescale(oracle.threshold(float(np.float32(p))))
+    check_grads([f64(t)[1] for t in (dq, dk, dv)], [g[1] for g in ref], "kv_len 400 batch",
+                GRAD_REL * r)
