@@ -119,6 +119,19 @@ bool make_strides(int B, int H, int N, int d, long long sb, long long sh, long l
     if (order[k] == 1) out->ph = k;
     if (order[k] == 2) out->pb = k;
   }
+  // Head and batch merge into one axis bh = b*H + h when one stride serves
+  // both (H = 1, B = 1, or sb = H * sh) and it lies above the rows.
+  const long long sn_eff = N > 1 ? sn : d;
+  long long sbh = -1;
+  if (static_cast<long long>(B) * H == 1)
+    sbh = static_cast<long long>(N) * sn_eff;
+  else if (H == 1)
+    sbh = sb;
+  else if (B == 1 || sb == static_cast<long long>(H) * sh)
+    sbh = sh;
+  out->merged = (sbh >= 0 && sn_eff >= d && sbh >= static_cast<long long>(N) * sn_eff) ? 1 : 0;
+  out->bh = sbh;
+  out->n_map = sn_eff;
   return true;
 }
 
@@ -133,14 +146,27 @@ size_t span_bytes(int B, int H, int N, int d, const Strides& s, size_t elem) {
   return static_cast<size_t>((B - 1) * s.b + (H - 1) * s.h + (N - 1) * s.n + d) * elem;
 }
 
-// A bf16 [B, H, N, d] tensor with strides `st` as a 4-D tensor map: dimension
-// 0 is d, dimensions 1..3 the row, head and batch axes in the order st gives;
-// box = 64 columns (128 bytes) x 128 rows x 1 x 1, 128-byte swizzle, zero
-// fill outside the tensor (ragged N).
+// A bf16 [B, H, N, d] tensor with strides `st` as a tensor map: 3-D (d, N,
+// B*H) when st.merged, else 4-D with dimension 0 = d and dimensions 1..3 the
+// row, head and batch axes in the order st gives; box = 64 columns (128 bytes)
+// x 128 rows (x 1 x 1), 128-byte swizzle, zero fill outside the tensor
+// (ragged N).
 bool encode_rows(CUtensorMap* map, const void* base, int B, int H, int N, int d,
                  const Strides& st) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
+  if (st.merged) {  // 3-D (d, N, B*H)
+    const cuuint64_t dims3[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                 static_cast<cuuint64_t>(B) * static_cast<cuuint64_t>(H)};
+    const cuuint64_t strides3[2] = {static_cast<cuuint64_t>(st.n_map) * 2,
+                                    static_cast<cuuint64_t>(st.bh) * 2};
+    const cuuint32_t box3[3] = {64, static_cast<cuuint32_t>(kBlock), 1};
+    const cuuint32_t estr3[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims3, strides3,
+              box3, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4];
   dims[0] = static_cast<cuuint64_t>(d);

@@ -394,10 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar_kvfull + kvs, 2 * L::kTile);
         uint8_t* kv = smem + L::kKV + kvs * 2 * L::kTile;
         for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_rows(kv + c * kChunk, &tm_k, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh % grid.H,
-                        x.bh / grid.H, grid.st);
+          tma_load_rows(kv + c * kChunk, &tm_k, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh, grid.H,
+                        grid.st);
           tma_load_rows(kv + L::kTile + c * kChunk, &tm_v, bar_kvfull + kvs, c * 64, x.j * kBlock,
-                        x.bh % grid.H, x.bh / grid.H, grid.st);
+                        x.bh, grid.H, grid.st);
         }
         ++t;
         for (int it = 0, i = x.i0; it < x.n_iter; ++it, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_rows(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
-                        i * kBlock, x.bh % grid.H, x.bh / grid.H, grid.st);
+                        i * kBlock, x.bh, grid.H, grid.st);
           const size_t roff = static_cast<size_t>(x.bh) * Npad + static_cast<size_t>(i) * kBlock;
           bulk_load(smem + L::kStat + qs * 1024, lse2 + roff, 512, bar_qfull + qs);
           bulk_load(smem + L::kStat + qs * 1024 + 512, delta + roff, 512, bar_qfull + qs);
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(bar_dofull + ds, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_rows(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
-                        i * kBlock, x.bh % grid.H, x.bh / grid.H, grid.st);
+                        i * kBlock, x.bh, grid.H, grid.st);
           do_issued = gq + 1;
         }
       }

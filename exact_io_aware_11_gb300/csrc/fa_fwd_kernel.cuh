@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           mbar_expect_tx(bar_qfull + qb, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_rows(smem + L::kQ + qb * L::kTile + c * kChunk, &tm_q, bar_qfull + qb, c * 64,
-                        (t ? it.qtB : it.qtA) * kBlock, it.bh % g.H, it.bh / g.H, g.st);
+                        (t ? it.qtB : it.qtA) * kBlock, it.bh, g.H, g.st);
           ++nq;
         }
         for (int j = 0; ok && j < it.uend; ++j) {
@@ -283,13 +283,13 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           mbar_expect_tx(bar_kfull + ks, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_rows(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
-                        j * kBlock, it.bh % g.H, it.bh / g.H, g.st);
+                        j * kBlock, it.bh, g.H, g.st);
           k_issued = u + 1;
           if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) { ok = false; break; }
           mbar_expect_tx(bar_vfull + vs, L::kTile);
           for (int c = 0; c < L::kChunks; ++c)
             tma_load_rows(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
-                        j * kBlock, it.bh % g.H, it.bh / g.H, g.st);
+                        j * kBlock, it.bh, g.H, g.st);
           v_issued = u + 1;
           ++u;
         }

@@ -18,12 +18,16 @@ constexpr int kBlock = 128;
 // Element strides of the [B, H, N, d] tensors of one call (q, k, v, o, dout,
 // dq, dk, dv share them): element (b, h, n, c) sits at b*b + h*h + n*n + c.
 // [B, H, N, d] row-major is {H*N*d, N*d, d}; [B, N, H, d] is {N*H*d, d, H*d}.
-// The tensor maps over these tensors are 4-D: d, then the row, head and batch
-// axes in order of increasing stride; pn, ph, pb give the positions (0..2
-// among dimensions 1..3) of the row, head and batch coordinates.
+// When head and batch merge into one problem axis bh = b*H + h of stride
+// s_bh above the rows ([B, H, N, d] row-major, padded rows), the tensor maps
+// are 3-D (d, N, B*H) and `merged` is set. Otherwise they are 4-D: d, then the
+// row, head and batch axes in order of increasing stride, and pn, ph, pb give
+// the positions (0..2 among dimensions 1..3) of those coordinates.
 struct Strides {
   long long b, h, n;
   int pn, ph, pb;
+  int merged;
+  long long bh, n_map;  // merged maps: strides of the bh and row axes
 };
 
 // Coordinates (dimensions 1..3) of row n of head h in batch b.

@@ -209,13 +209,17 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// 128 rows (starting at `row`) x 64 columns (starting at `x`) of head h,
-// batch b from a 4-D [B, H, N, d] map whose outer dimensions follow `st`.
+// 128 rows (starting at `row`) x 64 columns (starting at `x`) of problem
+// bh = b*H + h from a [B, H, N, d] tensor map laid out as `st` says.
 __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                              int x, int row, int h, int b, const Strides& st) {
-  int y0, y1, y2;
-  row_coords(st, row, h, b, y0, y1, y2);
-  tma_load_4d(dst, map, bar, x, y0, y1, y2);
+                                              int x, int row, int bh, int H, const Strides& st) {
+  if (st.merged) {
+    tma_load_3d(dst, map, bar, x, row, bh);
+  } else {
+    int y0, y1, y2;
+    row_coords(st, row, bh % H, bh / H, y0, y1, y2);
+    tma_load_4d(dst, map, bar, x, y0, y1, y2);
+  }
 }
 
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).

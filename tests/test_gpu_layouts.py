@@ -126,7 +126,12 @@ def test_every_option_at_once(fa, d, causal):
     drop = (p32, seed, off)
     o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, causal=causal,
                                   kv_len=kv.numpy(), block_mask=m, dropout=drop)
-    check_fwd(o, lse, o_ref, l_ref, f"all options d={d} causal={causal}", O_ATOL * r)
+    # O is stored in bf16: beyond the plain bar scaled by r, the rounding of
+    # the exact value itself (unit roundoff 2^-8 of |O|) can not be avoided
+    # once r |v| passes 2 (kv_len 2 rows with one key dropped give O = r v_j).
+    err = np.abs(f64(o) - o_ref)
+    assert np.all(err <= O_ATOL * r + 2.0 ** -8 * np.abs(o_ref)), err.max()
+    check_fwd(o, lse, o_ref, l_ref, f"all options d={d} causal={causal}", np.inf)
     ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, causal=causal,
                           kv_len=kv.numpy(), block_mask=m, dropout=drop)
     check_grads(g, ref, f"all options d={d} causal={causal}", GRAD_REL * r)
