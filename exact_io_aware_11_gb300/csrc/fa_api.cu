@@ -91,6 +91,7 @@ bool make_strides(int B, int H, int N, int d, long long sb, long long sh, long l
   long long top = d;
   for (int a = 0; a < 3; ++a) {
     if (st[a] < 0 || st[a] >= lim || (st[a] & 7)) return false;
+    if (ext[a] > 1 && st[a] > lim / ext[a]) return false;  // span beyond 2^36 elements
     if (ext[a] > 1 && st[a] * ext[a] > top) top = st[a] * ext[a];
   }
   if (top >= lim) return false;

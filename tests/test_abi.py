@@ -223,3 +223,15 @@ def test_attention_options_validated(L):
                        (dict(block_mask=m, causal=1, dropout_p=0.3), 3)]:
         opt = _opts(**kw)
         assert L.fa_attention_fwd(q, k, v, o, lse, 1, 1, 128, 64, ctypes.byref(opt), None) == expect, kw
+
+
+@needs_cpu
+def test_attention_strides_reject_huge_spans(L):
+    import ctypes
+    q, k, v, o, lse = ptrs(5)
+    # a row stride whose span over N rows passes 2^36 elements (and whose
+    # product with N would overflow 64 bits if it were formed unchecked)
+    opt = _opts(stride_b=0, stride_h=0, stride_n=(1 << 35))
+    assert L.fa_attention_fwd(q, k, v, o, lse, 1, 1, 1 << 30, 64, ctypes.byref(opt), None) == 1
+    opt = _opts(stride_b=(1 << 35) - 8, stride_h=64, stride_n=128)
+    assert L.fa_attention_fwd(q, k, v, o, lse, 4, 2, 16, 64, ctypes.byref(opt), None) == 1
