@@ -82,10 +82,18 @@ def ncu_traffic(kernel: str, workload: str):
     return nbytes if source_digest(src) == digest else None
 
 
-def flops(w: W.Workload, kv_len=None):
+def flops(w: W.Workload):
+    """Nominal fwd and bwd FLOPs: 4 B H N^2 d (halved for causal) and 2.5x that."""
     f = 4.0 * w.B * w.H * w.N * w.N * w.d
     if w.causal:
         f /= 2
+    return f, 2.5 * f
+
+
+def effective_flops(w: W.Workload, kv_len) -> tuple:
+    """FLOPs over the visible keys only, for key padding (non-causal):
+    sum over b of 4 H N len_b d, and 2.5x that."""
+    f = sum(4.0 * w.H * w.N * min(w.N, int(n)) * w.d for n in kv_len.tolist())
     return f, 2.5 * f
 
 
@@ -505,12 +513,18 @@ def sweep(fa, dev, flush, pk):
         r = {"fwd_ms": round(statistics.median(t["fwd"]), 4),
              "fwd_tflops": round(f_fwd / (statistics.median(t["fwd"]) * 1e-3) / 1e12, 2)}
         r["fwd_pct_peak"] = round(r["fwd_tflops"] / pk["bf16_tflops"], 4)
+        eff = None
+        if st.host["kv_len"] is not None and not w.causal:  # the kernels skip padded key tiles
+            eff = effective_flops(w, st.host["kv_len"])
+            r["fwd_tflops_effective"] = round(eff[0] / (r["fwd_ms"] * 1e-3) / 1e12, 2)
         if w.backward:
             mb = statistics.median([a + b + c for a, b, c in zip(t["bwd_pre"], t["bwd_main"],
                                                                    t["dq_convert"])])
             r["bwd_ms"] = round(mb, 4)
             r["bwd_tflops"] = round(f_bwd / (mb * 1e-3) / 1e12, 2)
             r["bwd_pct_peak"] = round(r["bwd_tflops"] / pk["bf16_tflops"], 4)
+            if eff is not None:
+                r["bwd_tflops_effective"] = round(eff[1] / (mb * 1e-3) / 1e12, 2)
             if w.sparse:
                 r["bwd_timing"] = "one fa_blocksparse_bwd call (preprocess, main, dQ convert)"
             elif w.dropout > 0:
