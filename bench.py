@@ -313,15 +313,17 @@ def time_steps(step: Step, steps: int, warmup: int, flush, backward=True, split=
     return times
 
 
-def e2e(fa, step: Step, steps: int, warmup: int):
-    """Same step through the public API with pinned host buffers; H2D of the
-    inputs and D2H of O, LSE, dQ, dK, dV inside the timed region."""
+def e2e_serial(fa, step: Step, steps: int, warmup: int):
+    """Same step through the public API with pinned host buffers, one step
+    after the other on one stream: H2D of the inputs, forward + backward, D2H
+    of O, LSE, dQ, dK, dV, all inside the timed region."""
     w = step.w
-    dev = step.q.device
     names = ["q", "k", "v", "dout"]
     host_in = {n: step.host[n].pin_memory() for n in names}
-    dev_in = {n: torch.empty_like(step.q) for n in names}
-    outs = [step.o, step.lse, step.dq, step.dk, step.dv]
+    dev = step.q.device
+    dev_in = {n: torch.empty(host_in[n].shape, dtype=host_in[n].dtype, device=dev) for n in names}
+    outs = [torch.empty(t.shape, dtype=t.dtype, device=dev)
+            for t in (step.o, step.lse, step.dq, step.dk, step.dv)]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     kv = step.kv
     stream = torch.cuda.current_stream()
@@ -330,10 +332,10 @@ def e2e(fa, step: Step, steps: int, warmup: int):
         for n in names:
             dev_in[n].copy_(host_in[n], non_blocking=True)
         o, lse = fa.forward(dev_in["q"], dev_in["k"], dev_in["v"], causal=w.causal, scale=w.scale,
-                            kv_len=kv, out=step.o, lse=step.lse)
+                            kv_len=kv, out=outs[0], lse=outs[1])
         fa.backward(dev_in["q"], dev_in["k"], dev_in["v"], o, dev_in["dout"], lse,
-                    causal=w.causal, scale=w.scale, kv_len=kv, workspace=step.ws, dq=step.dq,
-                    dk=step.dk, dv=step.dv)
+                    causal=w.causal, scale=w.scale, kv_len=kv, workspace=step.ws, dq=outs[2],
+                    dk=outs[3], dv=outs[4])
         for h, t in zip(host_out, outs):
             h.copy_(t, non_blocking=True)
 
@@ -350,6 +352,102 @@ def e2e(fa, step: Step, steps: int, warmup: int):
     h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in names)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     return ms, h2d, d2h
+
+
+def e2e_pipelined(fa, step: Step, steps: int, warmup: int):
+    """The same steps through the public API, software-pipelined as a training
+    or serving loop runs them: while step i computes on the compute stream, the
+    inputs of step i+1 upload on a copy stream and the results of step i-1
+    download on another (two sets of device buffers). Every step still copies
+    its inputs H2D from pinned memory and its O, LSE, dQ, dK, dV back D2H;
+    events order upload -> compute -> download of each step and keep a buffer
+    set from being overwritten before the step that used it is done. The timed
+    region runs from before the first upload to after the last download."""
+    w = step.w
+    dev = step.q.device
+    names = ["q", "k", "v", "dout"]
+    host_in = {n: step.host[n].pin_memory() for n in names}
+    dev_in = [{n: torch.empty(host_in[n].shape, dtype=host_in[n].dtype, device=dev)
+               for n in names} for _ in range(2)]
+    outs = [[torch.empty(t.shape, dtype=t.dtype, device=dev)
+             for t in (step.o, step.lse, step.dq, step.dk, step.dv)] for _ in range(2)]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs[0]]
+                for _ in range(2)]
+    kv = step.kv
+    comp = torch.cuda.current_stream(dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(n, start=None, end=None):
+        uploaded, computed, downloaded = [None] * n, [None] * n, [None] * n
+        if start is not None:
+            start.record(comp)
+        up.wait_stream(comp)
+        down.wait_stream(comp)
+        for i in range(n + 2):
+            if i < n:                                   # upload step i
+                s = i % 2
+                if i >= 2:
+                    up.wait_event(computed[i - 2])      # its buffers' last reader is done
+                with torch.cuda.stream(up):
+                    for nm in names:
+                        dev_in[s][nm].copy_(host_in[nm], non_blocking=True)
+                uploaded[i] = torch.cuda.Event()
+                uploaded[i].record(up)
+            j = i - 1
+            if 0 <= j < n:                              # compute step j
+                s = j % 2
+                comp.wait_event(uploaded[j])
+                if j >= 2:
+                    comp.wait_event(downloaded[j - 2])  # its outputs were copied out
+                o, lse, dq, dk, dv = outs[s]
+                x = dev_in[s]
+                fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, kv_len=kv,
+                           out=o, lse=lse, stream=comp)
+                fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=w.causal,
+                            scale=w.scale, kv_len=kv, workspace=step.ws, dq=dq, dk=dk, dv=dv,
+                            stream=comp)
+                computed[j] = torch.cuda.Event()
+                computed[j].record(comp)
+            j = i - 2
+            if 0 <= j < n:                              # download step j
+                s = j % 2
+                down.wait_event(computed[j])
+                with torch.cuda.stream(down):
+                    for h, t in zip(host_out[s], outs[s]):
+                        h.copy_(t, non_blocking=True)
+                downloaded[j] = torch.cuda.Event()
+                downloaded[j].record(down)
+        comp.wait_event(downloaded[n - 1])
+        if end is not None:
+            end.record(comp)
+
+    run(warmup)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(steps, a, b)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = sum(host_in[n].numel() * host_in[n].element_size() for n in names)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    # the last step downloaded the O of its own uploaded inputs
+    last = (steps - 1) % 2
+    o_chk, _ = fa.forward(dev_in[last]["q"], dev_in[last]["k"], dev_in[last]["v"],
+                          causal=w.causal, scale=w.scale, kv_len=kv)
+    torch.cuda.synchronize()
+    if not torch.equal(host_out[last][0], o_chk.cpu()):
+        raise RuntimeError("pipelined end-to-end step produced a different O")
+    return ms, h2d, d2h
+
+
+def e2e(fa, step: Step, steps: int, warmup: int):
+    """End-to-end timing through the public API: the pipelined schedule, or the
+    serial one if the pipelined run fails. Returns (ms per step, H2D bytes,
+    D2H bytes, schedule)."""
+    try:
+        return (*e2e_pipelined(fa, step, steps, warmup), "pipelined")
+    except Exception as exc:  # noqa: BLE001 -- report the serial schedule instead
+        torch.cuda.synchronize()
+        return (*e2e_serial(fa, step, steps, warmup), f"serial (pipelined failed: {exc})")
 
 
 def cpu_baseline(w: W.Workload, budget_s: float = 12.0):
@@ -462,7 +560,8 @@ def run_ours(args, world, rank, local):
                     "peak_kind": f"{pk_kind} bf16 dense (burst)",
                     "traffic": ncu_traffic(dom, w.name)}
 
-    e2e_ms, h2d, d2h = e2e(fa, step, max(3, args.steps // 4), 3) if w.backward else (None, 0, 0)
+    e2e_ms, h2d, d2h, e2e_sched = (e2e(fa, step, max(3, args.steps // 4), 3) if w.backward
+                                   else (None, 0, 0, None))
     clk = clocks.stop(window=tuple(t_region))
 
     out = {
@@ -490,7 +589,7 @@ def run_ours(args, world, rank, local):
         e2e_value, e2e_ms = whole_job_tflops(world, step_flops, e2e_ms)
         out["e2e"] = {"value": round(e2e_value, 3),
                       "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                      "ms_per_step": round(e2e_ms, 4)}
+                      "ms_per_step": round(e2e_ms, 4), "schedule": e2e_sched}
     if args.sweep and rank == 0:
         out["sweep"] = sweep(fa, dev, flush, pk)
     if rank == 0 and world == 1:
