@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -205,11 +206,18 @@ bool encode_f32_rows(CUtensorMap* map, const void* base, int BH, int rows, int d
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The kernels count work items (B*H*ceil(N/128)), problems (B*H) and padded
+// rows (N rounded up to 128) in 32-bit integers.
+bool sizes_fit_int(int B, int H, int N) {
+  if (N > INT_MAX - (kBlock - 1)) return false;
+  const long long tiles = (static_cast<long long>(N) + kBlock - 1) / kBlock;
+  return static_cast<long long>(B) * H * tiles <= INT_MAX;
+}
+
 int check_common(int B, int H, int N, int d, float scale) {
   if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * H > 65535LL * 65535LL) return FA_ERR_INVALID_ARG;
-  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535 || !sizes_fit_int(B, H, N)) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -472,7 +480,7 @@ int fa_dropout_mask(int B, int H, int N, float dropout_p, uint64_t seed, uint32_
   DropoutParams drop{};
   if (!make_dropout(dropout_p, seed, offset, &drop)) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1 || !keep) return FA_ERR_INVALID_ARG;
-  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535 || !sizes_fit_int(B, H, N)) return FA_ERR_INVALID_ARG;
   DeviceInfo dev;
   const int st = current_device_info(&dev);
   if (st != FA_OK) return st;

@@ -235,3 +235,13 @@ def test_attention_strides_reject_huge_spans(L):
     assert L.fa_attention_fwd(q, k, v, o, lse, 1, 1, 1 << 30, 64, ctypes.byref(opt), None) == 1
     opt = _opts(stride_b=(1 << 35) - 8, stride_h=64, stride_n=128)
     assert L.fa_attention_fwd(q, k, v, o, lse, 4, 2, 16, 64, ctypes.byref(opt), None) == 1
+
+
+@needs_cpu
+@pytest.mark.parametrize("B,H,N", [(65535, 65535, 128), (4096, 4096, 1 << 14), (1, 1, (1 << 31) - 1)])
+def test_sizes_beyond_32_bit_work_counts_rejected(L, B, H, N):
+    # B*H*ceil(N/128) work items (or N rounded up to whole tiles) past 2^31 - 1
+    q, k, v, o, lse, keep = ptrs(6)
+    assert L.fa_fwd(q, k, v, o, lse, B, H, N, 64, 0, 0.125, None) == 1
+    assert L.fa_dropout_mask(B, H, N, 0.1, 1, 0, keep, None) == 1
+
