@@ -28,6 +28,9 @@ SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P]),
     "fa_fwd_kpad": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P]),
     "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "fa_bwd_split_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "fa_fwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "fa_fwd_split": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P, ctypes.c_size_t, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _P, _P,
                     ctypes.c_size_t, _P]),
     "fa_bwd_preprocess": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
@@ -58,6 +61,9 @@ class AttentionOptions(ctypes.Structure):
 
 SIGNATURES["fa_attention_fwd"] = (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
                                        ctypes.POINTER(AttentionOptions), _P])
+SIGNATURES["fa_attention_fwd_split"] = (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                             ctypes.POINTER(AttentionOptions), _P, ctypes.c_size_t,
+                                             _P])
 SIGNATURES["fa_attention_bwd"] = (_I, [_P] * 9 + [_I, _I, _I, _I, ctypes.POINTER(AttentionOptions),
                                                   _P, ctypes.c_size_t, _P])
 
@@ -116,9 +122,44 @@ def _raise(rc: int, where: str):
         raise FaError(rc, where)
 
 
+def fwd_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool = False) -> int:
+    """Workspace bytes with which the forward splits its last wave (0: no split)."""
+    return int(lib().fa_fwd_workspace_bytes(B, H, N, d, int(bool(causal))))
+
+
+def bwd_split_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool = False) -> int:
+    """Backward workspace bytes that also enable the split of its last wave."""
+    return int(lib().fa_bwd_split_workspace_bytes(B, H, N, d, int(bool(causal))))
+
+
+def _bwd_workspace(q, causal, kv_len, block_mask, split, workspace):
+    if workspace is not None:
+        return workspace
+    B, H, N, d = q.shape
+    need = (bwd_split_workspace_bytes(B, H, N, d, causal)
+            if split and kv_len is None and block_mask is None else bwd_workspace_bytes(B, H, N, d))
+    return torch.empty(need, dtype=torch.uint8, device=q.device)
+
+
+def _fwd_workspace(q, causal, kv_len, block_mask, split, workspace):
+    """(pointer, bytes, tensor) of the forward's split workspace, or (None, 0, None)."""
+    if workspace is not None:
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size(), workspace
+    if not split or kv_len is not None or block_mask is not None:
+        return None, 0, None
+    B, H, N, d = q.shape
+    need = fwd_workspace_bytes(B, H, N, d, causal)
+    if need == 0:
+        return None, 0, None
+    ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    return ws.data_ptr(), need, ws
+
+
 def forward(q, k, v, causal: bool = False, scale: float | None = None, kv_len=None,
-            out=None, lse=None, stream=None):
-    """O, LSE = exact attention forward (fa_fwd / fa_fwd_kpad)."""
+            out=None, lse=None, stream=None, split: bool = True, workspace=None):
+    """O, LSE = exact attention forward (fa_fwd_split: fa_fwd_kpad, with the
+    last wave of work spread over every SM when that helps and split=True).
+    `workspace`: optional uint8 CUDA tensor of fwd_workspace_bytes(...) bytes."""
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -126,9 +167,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, kv_len=No
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     if kv_len is not None and (kv_len.dtype != torch.int32 or not kv_len.is_cuda):
         raise ValueError("kv_len must be a CUDA int32 tensor of shape [B]")
-    rc = lib().fa_fwd_kpad(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
-                           B, H, N, d, int(bool(causal)), scale, _ptr(kv_len), _stream_ptr(stream))
-    _raise(rc, "fa_fwd_kpad")
+    wp, wn, _ws = _fwd_workspace(q, causal, kv_len, None, split, workspace)
+    rc = lib().fa_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                            B, H, N, d, int(bool(causal)), scale, _ptr(kv_len), wp, wn,
+                            _stream_ptr(stream))
+    _raise(rc, "fa_fwd_split")
     return o, l
 
 
@@ -157,14 +200,16 @@ def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 
 def backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
-             kv_len=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+             kv_len=None, workspace=None, dq=None, dk=None, dv=None, stream=None,
+             split: bool = True):
     """dQ, dK, dV of L = sum(dout * O) (fa_bwd). `workspace` is an optional
-    uint8 CUDA tensor of at least bwd_workspace_bytes(...) bytes."""
+    uint8 CUDA tensor of at least bwd_workspace_bytes(...) bytes (with
+    bwd_split_workspace_bytes(...) or more the last wave is split over every
+    SM); without one, the split size is allocated unless split=False."""
     _check_qkv(q, k, v, o, dout)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    need = bwd_workspace_bytes(B, H, N, d)
-    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    ws = _bwd_workspace(q, causal, kv_len, None, split, workspace)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
@@ -239,8 +284,7 @@ def dropout_backward(q, k, v, o, dout, lse, dropout_p: float, seed: int, offset:
     p, seed, offset = _check_dropout(dropout_p, seed, offset)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    need = bwd_workspace_bytes(B, H, N, d)
-    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    ws = _bwd_workspace(q, causal, kv_len, None, True, workspace)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
@@ -303,7 +347,8 @@ def _options(q, causal, scale, kv_len, block_mask, block_size, dropout_p, seed, 
 
 def attention_forward(q, k, v, causal: bool = False, scale: float | None = None, kv_len=None,
                       block_mask=None, block_size: int = 128, dropout_p: float = 0.0,
-                      seed: int = 0, offset: int = 0, out=None, lse=None, stream=None):
+                      seed: int = 0, offset: int = 0, out=None, lse=None, stream=None,
+                      split: bool = True, workspace=None):
     """O, LSE with every option at once (fa_attention_fwd). q, k, v are
     [B, H, N, d] views sharing one set of strides -- e.g. x.transpose(1, 2) of
     a [B, N, H, d] tensor; O is returned with the same strides."""
@@ -313,23 +358,24 @@ def attention_forward(q, k, v, causal: bool = False, scale: float | None = None,
     o = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) if out is None else out
     _check_views(q, o)
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    rc = lib().fa_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                l.data_ptr(), B, H, N, d, ctypes.byref(opt), _stream_ptr(stream))
-    _raise(rc, "fa_attention_fwd")
+    wp, wn, _ws = _fwd_workspace(q, causal, kv_len, block_mask, split, workspace)
+    rc = lib().fa_attention_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      l.data_ptr(), B, H, N, d, ctypes.byref(opt), wp, wn,
+                                      _stream_ptr(stream))
+    _raise(rc, "fa_attention_fwd_split")
     return o, l
 
 
 def attention_backward(q, k, v, o, dout, lse, causal: bool = False, scale: float | None = None,
                        kv_len=None, block_mask=None, block_size: int = 128,
                        dropout_p: float = 0.0, seed: int = 0, offset: int = 0, workspace=None,
-                       dq=None, dk=None, dv=None, stream=None):
+                       dq=None, dk=None, dv=None, stream=None, split: bool = True):
     """dQ, dK, dV of attention_forward with the same options (fa_attention_bwd);
     the gradients have the inputs' strides."""
     _check_views(q, k, v, o, dout)
     B, H, N, d = q.shape
     opt = _options(q, causal, scale, kv_len, block_mask, block_size, dropout_p, seed, offset)
-    need = bwd_workspace_bytes(B, H, N, d)
-    ws = torch.empty(need, dtype=torch.uint8, device=q.device) if workspace is None else workspace
+    ws = _bwd_workspace(q, causal, kv_len, block_mask, split, workspace)
 
     def like():
         return torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)

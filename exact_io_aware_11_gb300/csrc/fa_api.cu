@@ -13,6 +13,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "fa_sched.cuh"
 
 namespace fa {
 
@@ -143,6 +144,49 @@ bool dense_strides(int B, int H, int N, int d, Strides* s) {
                       d, s);
 }
 
+// Whether two bf16 [B, H, N, d] tensors with the same strides `s` share an
+// element, their bases `a` and `b` (16-byte aligned) being given. Row starts
+// form the set P = {i_b sb + i_h sh + i_n sn}; the tensors overlap iff the
+// base difference (in elements) lies within d - 1 of some difference of two
+// row starts, sum_a k_a s_a with |k_a| < extent_a. The axes' strides nest
+// (each at least the one below times its extent, as make_strides requires),
+// so for every axis, largest stride first, only the coefficients next to
+// delta / stride can lead to a hit, and a search over those is exact. This
+// accepts interleaved views such as q, k, v of one packed [B, N, 3, H, d]
+// buffer, which a comparison of address spans would reject.
+bool strided_overlap(const void* a, const void* b, int B, int H, int N, int d, const Strides& s) {
+  const long long diff = static_cast<long long>(reinterpret_cast<uintptr_t>(b)) -
+                         static_cast<long long>(reinterpret_cast<uintptr_t>(a));
+  if (diff % 2 != 0) return true;  // not on the same element grid: be conservative
+  const long long delta = diff / 2;
+  long long st[3] = {s.n, s.h, s.b}, ext[3] = {N, H, B};
+  // axes of extent 1 never step; sort the rest by stride, largest first
+  int ord[3] = {0, 1, 2};
+  for (int x = 0; x < 3; ++x)
+    for (int y = 0; y + 1 < 3 - x; ++y)
+      if (st[ord[y]] < st[ord[y + 1]]) {
+        const int t = ord[y];
+        ord[y] = ord[y + 1];
+        ord[y + 1] = t;
+      }
+  struct Rec {
+    static bool hit(const long long* st, const long long* ext, const int* ord, int lvl, long long r,
+                    int d) {
+      if (lvl == 3) return r > -d && r < d;
+      const int ax = ord[lvl];
+      if (ext[ax] <= 1 || st[ax] == 0) return hit(st, ext, ord, lvl + 1, r, d);
+      const long long lim = ext[ax] - 1;
+      long long k0 = r / st[ax];
+      for (long long k = k0 - 1; k <= k0 + 1; ++k) {
+        if (k < -lim || k > lim) continue;
+        if (hit(st, ext, ord, lvl + 1, r - k * st[ax], d)) return true;
+      }
+      return false;
+    }
+  };
+  return Rec::hit(st, ext, ord, 0, delta, d);
+}
+
 // Bytes from the first to one past the last element of a tensor with strides s.
 size_t span_bytes(int B, int H, int N, int d, const Strides& s, size_t elem) {
   return static_cast<size_t>((B - 1) * s.b + (H - 1) * s.h + (N - 1) * s.n + d) * elem;
@@ -245,7 +289,8 @@ size_t tensor_bytes(int B, int H, int N, int d, size_t elem) {
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int N, int d, int causal, float scale, const int32_t* kv_len,
                const uint8_t* block_mask, cudaStream_t stream,
-               const DropoutParams* drop = nullptr, const Strides* strides = nullptr) {
+               const DropoutParams* drop = nullptr, const Strides* strides = nullptr,
+               void* split_ws = nullptr, size_t split_ws_bytes = 0) {
   int st = check_common(B, H, N, d, scale);
   if (st != FA_OK) return st;
   Strides lay{};
@@ -258,11 +303,16 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_INVALID_ARG;
   if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  if (split_ws != nullptr && !aligned16(split_ws)) return FA_ERR_INVALID_ARG;
   const size_t tb = span_bytes(B, H, N, d, lay, 2), lb = tensor_bytes(B, H, N, 1, 4);
   const void* ins[3] = {q, k, v};
   for (const void* in : ins)
-    if (overlaps(o, tb, in, tb) || overlaps(lse, lb, in, tb)) return FA_ERR_INVALID_ARG;
+    if (strided_overlap(o, in, B, H, N, d, lay) || overlaps(lse, lb, in, tb) ||
+        (split_ws && overlaps(split_ws, split_ws_bytes, in, tb)))
+      return FA_ERR_INVALID_ARG;
   if (overlaps(o, tb, lse, lb)) return FA_ERR_INVALID_ARG;
+  if (split_ws && (overlaps(split_ws, split_ws_bytes, o, tb) || overlaps(split_ws, split_ws_bytes, lse, lb)))
+    return FA_ERR_INVALID_ARG;
   DeviceInfo dev;
   st = current_device_info(&dev);
   if (st != FA_OK) return st;
@@ -283,6 +333,8 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   a.kv_len = kv_len;
   a.block_mask = block_mask;
   if (drop) a.drop = *drop;
+  a.split_ws = split_ws;
+  a.split_ws_bytes = split_ws ? split_ws_bytes : 0;
   a.status = dev.status;
   a.wait_limit = kWaitLimitCycles;
   return launch_fwd(a, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -326,7 +378,12 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
     if (x && !aligned16(x)) return FA_ERR_INVALID_ARG;
   if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
   const BwdWorkspace ws = bwd_workspace_layout(B, H, N, d);
-  if (workspace_bytes < ws.total) return FA_ERR_INVALID_ARG;
+  if (ws.total == 0 || workspace_bytes < ws.total) return FA_ERR_INVALID_ARG;
+  // The split area (fa_bwd_split_workspace_bytes) follows the base regions;
+  // the main kernel uses it only if it is complete.
+  const size_t split_bytes = bwd_split_layout(sm_count(), d).total;
+  const bool have_split = workspace_bytes - ws.total >= split_bytes;
+  const size_t ws_used = ws.total + (have_split ? split_bytes : 0);
   const size_t tb = span_bytes(B, H, N, d, lay, 2), lb = tensor_bytes(B, H, N, 1, 4);
   const void* ins[] = {p.q, p.k, p.v, p.o, p.dout};
   void* outs[] = {p.dq, p.dk, p.dv};
@@ -334,15 +391,15 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
     void* out = outs[x];
     if (!out) continue;
     for (const void* in : ins)
-      if (in && overlaps(out, tb, in, tb)) return FA_ERR_INVALID_ARG;
-    if ((p.lse && overlaps(out, tb, p.lse, lb)) || overlaps(out, tb, p.ws, ws.total))
+      if (in && strided_overlap(out, in, B, H, N, d, lay)) return FA_ERR_INVALID_ARG;
+    if ((p.lse && overlaps(out, tb, p.lse, lb)) || overlaps(out, tb, p.ws, ws_used))
       return FA_ERR_INVALID_ARG;
     for (int y = x + 1; y < 3; ++y)
-      if (outs[y] && overlaps(out, tb, outs[y], tb)) return FA_ERR_INVALID_ARG;
+      if (outs[y] && strided_overlap(out, outs[y], B, H, N, d, lay)) return FA_ERR_INVALID_ARG;
   }
   for (const void* in : ins)
-    if (in && overlaps(p.ws, ws.total, in, tb)) return FA_ERR_INVALID_ARG;
-  if (p.lse && overlaps(p.ws, ws.total, p.lse, lb)) return FA_ERR_INVALID_ARG;
+    if (in && overlaps(p.ws, ws_used, in, tb)) return FA_ERR_INVALID_ARG;
+  if (p.lse && overlaps(p.ws, ws_used, p.lse, lb)) return FA_ERR_INVALID_ARG;
   DeviceInfo dev;
   st = current_device_info(&dev);
   if (st != FA_OK) return st;
@@ -372,6 +429,8 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
   a.kv_len = kv_len;
   a.block_mask = block_mask;
   if (drop) a.drop = *drop;
+  a.split_ws = have_split ? wsb + ws.total : nullptr;
+  a.split_ws_bytes = have_split ? split_bytes : 0;
   a.dq_acc = reinterpret_cast<float*>(wsb + ws.dq_off);
   a.lse2 = reinterpret_cast<float*>(wsb + ws.lse2_off);
   a.delta = reinterpret_cast<float*>(wsb + ws.delta_off);
@@ -384,7 +443,7 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
 
 BwdWorkspace bwd_workspace_layout(int B, int H, int N, int d) {
   BwdWorkspace w{};
-  const size_t npad = static_cast<size_t>((N + kBlock - 1) / kBlock) * kBlock;
+  const size_t npad = (static_cast<size_t>(N) + kBlock - 1) / kBlock * kBlock;
   const size_t rows = static_cast<size_t>(B) * H * npad;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   w.dq_off = 0;
@@ -433,7 +492,32 @@ int fa_blocksparse_fwd(const void* q, const void* k, const void* v, void* o, flo
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  if (B > 65535 || H > 65535 || !sizes_fit_int(B, H, N)) return 0;
   return bwd_workspace_layout(B, H, N, d).total;
+}
+
+size_t fa_bwd_split_workspace_bytes(int B, int H, int N, int d, int causal) {
+  const size_t base = fa_bwd_workspace_bytes(B, H, N, d);
+  if (base == 0 || (causal != 0 && causal != 1)) return 0;
+  const int G = sm_count();
+  const SplitPlan p = plan_bwd(B, H, N, d, causal != 0, G, true);
+  return p.whole < p.n_items ? base + bwd_split_layout(G, d).total : base;
+}
+
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1)) return 0;
+  if (B > 65535 || H > 65535 || !sizes_fit_int(B, H, N)) return 0;
+  const int G = sm_count();
+  const SplitPlan p = plan_fwd(B, H, N, d, causal != 0, G, true);
+  return p.whole < p.n_items ? fwd_split_layout(G, d).total : 0;
+}
+
+int fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, const int32_t* kv_len, void* workspace,
+                 size_t workspace_bytes, struct CUstream_st* stream) {
+  if (workspace == nullptr && workspace_bytes != 0) return FA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, H, N, d, causal, scale, kv_len, nullptr, stream, nullptr,
+                    nullptr, workspace, workspace_bytes);
 }
 
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -518,6 +602,20 @@ int fa_attention_fwd(const void* q, const void* k, const void* v, void* o, float
   if (st != FA_OK) return st;
   return fwd_common(q, k, v, o, lse, B, H, N, d, opt->causal, opt->scale, opt->kv_len,
                     opt->block_mask, stream, use_drop ? &drop : nullptr, &lay);
+}
+
+int fa_attention_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, const fa_attention_options* opt,
+                           void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  Strides lay{};
+  DropoutParams drop{};
+  bool use_drop = false;
+  const int st = attention_options(opt, B, H, N, d, &lay, &drop, &use_drop);
+  if (st != FA_OK) return st;
+  if (workspace == nullptr && workspace_bytes != 0) return FA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, H, N, d, opt->causal, opt->scale, opt->kv_len,
+                    opt->block_mask, stream, use_drop ? &drop : nullptr, &lay, workspace,
+                    workspace_bytes);
 }
 
 int fa_attention_bwd(const void* q, const void* k, const void* v, const void* o,

@@ -1,8 +1,9 @@
 // Backward pass of exact attention: the preprocess and dQ-conversion stages,
-// the dense (causal or not, key-padded or not) variants of the main kernel
-// (fa_bwd_kernel.cuh) and the watchdog self-test kernel. The block-sparse and
-// dropout variants of the main kernel are compiled in fa_bwd_sparse.cu,
-// fa_bwd_dropout.cu and fa_bwd_dropout_sparse.cu.
+// the planning of the main stage, the plain (dense, causal or not, key-padded
+// or not) variants of the main kernel (fa_bwd_kernel.cuh) and the watchdog
+// self-test kernel. The block-sparse, dropout and split variants of the main
+// kernel are compiled in fa_bwd_sparse.cu, fa_bwd_dropout.cu,
+// fa_bwd_dropout_sparse.cu and fa_bwd_split.cu.
 #include "fa_bwd_kernel.cuh"
 
 namespace fa {
@@ -22,47 +23,80 @@ __global__ void wait_selftest_kernel(int* status, long long limit) {
   if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, wd);
 }
 
+// Blocks of 256 threads for a grid-stride kernel over `threads` work items:
+// at most 16 resident blocks per SM.
 int grid_for(long long threads) {
   long long blocks = (threads + 255) / 256;
-  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  const long long cap = static_cast<long long>(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
   return static_cast<int>(blocks < 1 ? 1 : blocks);
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch_bwd_t(const BwdLaunch& a, int stages, cudaStream_t stream) {
-  const int BH = a.B * a.H;
-  const int nt = (a.N + kBlock - 1) / kBlock;
-  const int Npad = nt * kBlock;
-  cudaError_t e = cudaSuccess;
-  if (stages & kBwdStagePre) {
-    e = launch_pdl(bwd_pre_kernel<D>, dim3(grid_for(static_cast<long long>(BH) * Npad * (D / 8))),
-                   dim3(256), 0, stream, a.o, a.dout, a.lse, a.lse2, a.delta, a.dq_acc, BH, a.N,
-                   Npad, a.st, a.H);
-    if (e != cudaSuccess) return e;
+template <int D>
+cudaError_t launch_pre(const BwdLaunch& a, int BH, int Npad, cudaStream_t stream) {
+  return launch_pdl(bwd_pre_kernel<D>, dim3(grid_for(static_cast<long long>(BH) * Npad * (D / 8))),
+                    dim3(256), 0, stream, a.o, a.dout, a.lse, a.lse2, a.delta, a.dq_acc, BH, a.N,
+                    Npad, a.st, a.H);
+}
+
+template <int D>
+cudaError_t launch_convert(const BwdLaunch& a, int BH, int Npad, cudaStream_t stream) {
+  return launch_pdl(dq_convert_kernel<D>, dim3(grid_for(static_cast<long long>(BH) * a.N * (D / 8))),
+                    dim3(256), 0, stream, a.dq_acc, a.dq, BH, a.N, Npad, a.st, a.H);
+}
+
+// The main stage: plans the work (which items, whether the last wave is
+// split) and launches the variant it needs.
+cudaError_t launch_main(const BwdLaunch& a, cudaStream_t stream) {
+  BwdGrid g{};
+  g.H = a.H;
+  g.N = a.N;
+  g.nt = (a.N + kBlock - 1) / kBlock;
+  g.BH = a.B * a.H;
+  g.n_items = g.BH * g.nt;
+  g.kv_len = a.kv_len;
+  g.mask = a.block_mask;
+  g.st = a.st;
+  const int sms = sm_count();
+  const BwdSplitWorkspace ws = bwd_split_layout(sms, a.d);
+  const bool allowed = a.split_ws != nullptr && a.split_ws_bytes >= ws.total && a.kv_len == nullptr &&
+                       a.block_mask == nullptr;
+  g.plan = plan_bwd(a.B, a.H, a.N, a.d, a.causal != 0, sms, allowed);
+  if (g.plan.whole < g.plan.n_items) {
+    uint8_t* w = static_cast<uint8_t*>(a.split_ws);
+    g.slot_item = reinterpret_cast<int*>(w + ws.slot_off);
+    g.dkv_part = reinterpret_cast<float*>(w + ws.dkv_off);
+    return launch_bwd_main_split(a, g, sms, stream);
   }
-  if (stages & kBwdStageMain) {
-    if (a.drop.enabled)
-      e = launch_bwd_main_dropout(a, stream);
-    else if (a.block_mask != nullptr)
-      e = launch_bwd_main_sparse(a, stream);
-    else
-      e = launch_bwd_main_t<D, CAUSAL, false, false>(a, stream);
-    if (e != cudaSuccess) return e;
-  }
-  if (stages & kBwdStageConvert) {
-    e = launch_pdl(dq_convert_kernel<D>, dim3(grid_for(static_cast<long long>(BH) * a.N * (D / 8))),
-                   dim3(256), 0, stream, a.dq_acc, a.dq, BH, a.N, Npad, a.st, a.H);
-  }
-  return e;
+  const int grid = min(g.n_items, sms);
+  if (a.block_mask != nullptr)
+    return a.drop.enabled ? launch_bwd_main_dropout_sparse(a, g, grid, stream)
+                          : launch_bwd_main_sparse(a, g, grid, stream);
+  if (a.drop.enabled) return launch_bwd_main_dropout(a, g, grid, stream);
+  return launch_bwd_main_plain(a, g, grid, stream);
 }
 
 }  // namespace
 
+cudaError_t launch_bwd_main_plain(const BwdLaunch& a, const BwdGrid& g, int grid, cudaStream_t stream) {
+  return launch_bwd_main_variant<kModePlain, false>(a, g, grid, stream);
+}
+
 cudaError_t launch_bwd(const BwdLaunch& a, int stages, cudaStream_t stream) {
-  const bool causal = a.causal != 0;
-  if (a.d == 64)
-    return causal ? launch_bwd_t<64, true>(a, stages, stream) : launch_bwd_t<64, false>(a, stages, stream);
-  return causal ? launch_bwd_t<128, true>(a, stages, stream) : launch_bwd_t<128, false>(a, stages, stream);
+  const int BH = a.B * a.H;
+  const int Npad = (a.N + kBlock - 1) / kBlock * kBlock;
+  cudaError_t e = cudaSuccess;
+  if (stages & kBwdStagePre) {
+    e = a.d == 64 ? launch_pre<64>(a, BH, Npad, stream) : launch_pre<128>(a, BH, Npad, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kBwdStageMain) {
+    e = launch_main(a, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (stages & kBwdStageConvert)
+    e = a.d == 64 ? launch_convert<64>(a, BH, Npad, stream) : launch_convert<128>(a, BH, Npad, stream);
+  return e;
 }
 
 cudaError_t launch_wait_selftest(int* status, long long limit_cycles, cudaStream_t stream) {

@@ -8,14 +8,9 @@
 
 namespace fa {
 
-cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, cudaStream_t stream) {
-  if (a.block_mask != nullptr) return launch_bwd_main_dropout_sparse(a, stream);
-  const bool causal = a.causal != 0;
-  if (a.d == 64)
-    return causal ? launch_bwd_main_t<64, true, false, true>(a, stream)
-                  : launch_bwd_main_t<64, false, false, true>(a, stream);
-  return causal ? launch_bwd_main_t<128, true, false, true>(a, stream)
-                : launch_bwd_main_t<128, false, false, true>(a, stream);
+cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, const BwdGrid& g, int grid,
+                                    cudaStream_t stream) {
+  return launch_bwd_main_variant<kModePlain, true>(a, g, grid, stream);
 }
 
 }  // namespace fa

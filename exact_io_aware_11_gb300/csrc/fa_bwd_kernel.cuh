@@ -40,6 +40,7 @@
 #include "fa_internal.h"
 #include "fa_philox.cuh"
 #include "fa_ptx.cuh"
+#include "fa_sched.cuh"
 
 namespace fa {
 namespace {
@@ -63,7 +64,7 @@ struct BwdLayout {
   static constexpr int kDSb = kStat + kQS * 1024;    // dS^T, bf16, 2 chunks
   static constexpr int kDQ = kDSb + 2 * kChunk;      // dQ staging (fp32, 128-byte swizzle)
   static constexpr int kBar = kDQ + kDQChunks * kChunk;
-  static constexpr int kEnd = kBar + 256;
+  static constexpr int kEnd = kBar + 512 + 14 * 128;  // barriers etc.; tile lists of the 14 warps
   static constexpr int kSmem = kEnd + 1024;
   // TMEM columns
   static constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256, kTDK = 256 + D;
@@ -190,82 +191,60 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
 }
 
 // ----------------------------------------------------------------- work items
-// One work item: key tile j of one (batch, head), met by Q tiles i0 .. nt-1.
-// An item whose keys all lie beyond the valid length has no iterations; its
-// dK and dV rows are written as zeros.
-struct BwdGrid {
-  int H, N, nt, BH, n_items;
-  Strides st;  // of q, k, v, dout, dk, dv
-  const int32_t* kv_len;
-  const uint8_t* mask;  // block-sparse: uint8 [nt][nt], nonzero = (query tile, key tile) kept
-};
-
+// One work unit: key tile j of one (batch, head), met by the Q tiles of
+// steps [sb, se) of its item (Q tiles i0 + sb .. i0 + se - 1 without a block
+// mask; with one, the kept Q tiles). A unit whose keys all lie beyond the
+// valid length has no iterations; its dK and dV rows are written as zeros.
+// `slot` >= 0: the unit is part of a split item and its dK, dV go to that
+// workspace slot for the merge kernel.
 struct BwdItem {
-  int bh, j, i0, n_iter, kv_bound;  // i0: first query tile met (the rest follow bwd_next_row)
+  int bh, j, n_iter, kv_bound, slot;
+  TileSet ts;  // the Q tiles met
 };
 
-template <bool SPARSE>
-__device__ __forceinline__ int bwd_next_row(const BwdGrid& g, int j, int i);
+template <bool CAUSAL>
+__host__ __device__ __forceinline__ int bwd_steps(const BwdGrid& g, int k) {
+  return bwd_item_steps(g.nt, g.BH, CAUSAL, k);
+}
 
-// Item k. Causal items are ordered heaviest first (key tile j meets nt - j
-// query tiles); otherwise a head's key tiles are consecutive, so that CTAs
-// running at the same time stream the same Q and dO tiles through L2.
-template <bool CAUSAL, bool SPARSE = false>
-__device__ __forceinline__ BwdItem make_bwd_item(const BwdGrid& g, int k) {
+// Unit u's item. With a block mask, counting the kept Q tiles is
+// warp-collective, so every lane of the calling warp must take part.
+template <bool CAUSAL, int MODE>
+__device__ __forceinline__ BwdItem make_bwd_item(const BwdGrid& g, const Unit& u) {
+  constexpr bool SPARSE = MODE == kModeSparse;
   BwdItem x;
-  if (CAUSAL) {
-    x.j = k / g.BH;
-    x.bh = k - x.j * g.BH;
-  } else {
-    x.bh = k / g.nt;
-    x.j = k - x.bh * g.nt;
-  }
+  bwd_item_coords(g.nt, g.BH, CAUSAL, u.k, x.bh, x.j);
+  x.slot = u.slot;
   x.kv_bound = g.N;
   if (g.kv_len != nullptr) x.kv_bound = min(g.N, max(0, g.kv_len[x.bh / g.H]));
-  x.i0 = CAUSAL ? x.j : 0;
-  x.n_iter = x.j * kBlock < x.kv_bound ? g.nt - x.i0 : 0;
-  if constexpr (SPARSE) {  // the query tiles (i >= j if causal) whose mask row keeps key tile j
-    int n = 0;
-    for (int i = x.i0; i < g.nt; ++i) n += g.mask[static_cast<size_t>(i) * g.nt + x.j] != 0;
-    x.n_iter = x.j * kBlock < x.kv_bound ? n : 0;
-    x.i0 = bwd_next_row<true>(g, x.j, x.i0);
+  const int i0 = CAUSAL ? x.j : 0;
+  x.ts = TileSet{i0 + u.sb, min(g.nt, i0 + u.se), SPARSE ? g.mask + x.j : nullptr, g.nt};
+  int n = x.ts.end - x.ts.begin;
+  if constexpr (SPARSE) {
+    TileWalk<> w;
+    w.init(x.ts);
+    n = w.count();
   }
+  x.n_iter = x.j * kBlock < x.kv_bound ? n : 0;
   return x;
 }
 
-// The first query tile >= i that meets key tile j: i itself unless a block
-// mask says otherwise (nt if there is none).
-template <bool SPARSE>
-__device__ __forceinline__ int bwd_next_row(const BwdGrid& g, int j, int i) {
-  if constexpr (SPARSE) {
-    while (i < g.nt && g.mask[static_cast<size_t>(i) * g.nt + j] == 0) ++i;
-  }
-  return i;
-}
-
-// The r-th item of this CTA: a snake over the item list; -1 when there is none.
-__device__ __forceinline__ int bwd_item_of(const BwdGrid& g, int r) {
-  const int G = gridDim.x, c = blockIdx.x;
-  if (r * G >= g.n_items) return -1;
-  const int k = r * G + ((r & 1) ? G - 1 - c : c);
-  return k < g.n_items ? k : -1;
-}
-
 // Position of the MMA issuer in this CTA's flattened sequence of iterations:
-// iteration `it` of `n` of the t-th item that has iterations, the g-th
+// iteration `it` of `n` of the t-th unit that has iterations, the g-th
 // iteration overall (ring slots and barrier phases follow t and g).
-template <bool CAUSAL, bool SPARSE>
+template <bool CAUSAL, int MODE>
 struct BwdCursor {
   int r = 0, it = 0, n = 0, t = 0, g = 0;
   bool valid = false;
-  __device__ void seek(const BwdGrid& G) {
+  template <typename UnitFn>
+  __device__ void seek(const BwdGrid& G, UnitFn unit) {
     for (;; ++r) {
-      const int k = bwd_item_of(G, r);
-      if (k < 0) {
+      const Unit u = unit(r);
+      if (u.k < 0) {
         valid = false;
         return;
       }
-      const int n_iter = make_bwd_item<CAUSAL, SPARSE>(G, k).n_iter;
+      const int n_iter = make_bwd_item<CAUSAL, MODE>(G, u).n_iter;
       if (n_iter > 0) {
         n = n_iter;
         it = 0;
@@ -274,12 +253,13 @@ struct BwdCursor {
       }
     }
   }
-  __device__ void next(const BwdGrid& G) {
+  template <typename UnitFn>
+  __device__ void next(const BwdGrid& G, UnitFn unit) {
     ++g;
     if (++it < n) return;
     ++t;
     ++r;
-    seek(G);
+    seek(G, unit);
   }
 };
 
@@ -291,7 +271,11 @@ struct BwdCursor {
 // DROP: dropout (fa_philox.cuh) regenerated from the element indices: dV is
 // accumulated from the dropped P^T (its 1 / (1 - p') applied when dV leaves
 // TMEM) and dS = P * (Z dP_dropped / (1 - p') - D).
-template <int D, bool CAUSAL, bool SPARSE, bool DROP>
+// MODE (kModePlain, kModeSparse, kModeSplit): the variant compiled -- dense
+// Q-tile ranges over whole items, the Q tiles a block mask keeps, or dense
+// ranges with the last wave's items cut into parts whose dK, dV go to the
+// workspace for the merge kernel.
+template <int D, bool CAUSAL, int MODE, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -324,6 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
   int* abort_flag = reinterpret_cast<int*>(bars + 24);
   uint64_t* bar_dpfree = bars + 25;   // dP^T read out of TMEM (d = 64)
+  TailRange* tail_sh = reinterpret_cast<TailRange*>(bars + 26);  // this CTA's share of a split tail
+  uint8_t* walk_list = reinterpret_cast<uint8_t*>(bars + 64);     // [warp][128] Q tiles of a window (sparse)
   // d = 64: dQ has TMEM columns of its own, so dP^T of the next Q tile can be
   // issued as soon as the compute warps have read dP^T of this one, ahead of
   // this tile's dK and dQ MMAs in the in-order tensor pipe.
@@ -366,6 +352,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  auto steps = [&](int k) { return bwd_steps<CAUSAL>(grid, k); };
+  if constexpr (MODE == kModeSplit) {
+    if (warp == 8) {
+      const TailRange tr = tail_range(grid.plan, blockIdx.x, gridDim.x, steps);
+      if (lane == 0) *tail_sh = tr;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -373,53 +366,110 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
   grid_dep_launch();
   const Watchdog wd{wait_limit, status, abort_flag};
+  if constexpr (MODE == kModeSplit) {
+    if (threadIdx.x == 0) {
+      const TailRange tr = *tail_sh;
+      write_slot_items(grid.slot_item, tr, blockIdx.x, tr.t1 >= tr.t0 ? steps(tr.t0) : 0,
+                       tr.t1 >= tr.t0 ? steps(tr.t1) : 0);
+    }
+  }
+  // The r-th unit of this CTA, or a unit with k < 0: whole items in a snake
+  // over the item list, and for a split plan the parts of its tail.
+  auto unit = [&](int r) -> Unit {
+    if constexpr (MODE == kModeSplit) {
+      return unit_of(grid.plan, tail_sh, r, blockIdx.x, gridDim.x, steps);
+    } else {
+      Unit u{-1, 0, 1 << 30, -1};
+      const int G = gridDim.x, c = blockIdx.x;
+      if (r * G >= grid.n_items) return u;
+      const int k = r * G + ((r & 1) ? G - 1 - c : c);
+      if (k < grid.n_items) u.k = k;
+      return u;
+    }
+  };
+  // The Q tiles of a unit, window by window: without a block mask one run
+  // [begin, end); with one, each 128-tile window's kept tiles are listed in
+  // the warp's shared-memory list. Returns the tiles of window w0 and sets
+  // `base` (tile = base + idx) or lists them (tile = w0 + list[idx]).
+  uint8_t* list = walk_list + 128 * warp;
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer (one lane)
+    // ------------------------------------------------------------ TMA producer
+    // Lane 0 waits for free ring slots and issues the copies (with a block
+    // mask the whole warp first lists each window's Q tiles).
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
       tma_prefetch_desc(&tm_dqacc);
-      int t = 0, q_issued = 0, do_issued = 0;
-      bool ok = true;
+    }
+    int t = 0, q_issued = 0, do_issued = 0;
+    bool ok = true;
+    // K_j, V_j of a unit into the next K/V stage (lane 0); false on an abort.
+    auto load_kv = [&](const BwdItem& x) -> bool {
+      const int kvs = t % KVS;
+      if (t >= KVS && !mbar_wait(bar_kvempty + kvs, ((t / KVS) - 1) & 1, wd)) return false;
+      mbar_expect_tx(bar_kvfull + kvs, 2 * L::kTile);
+      uint8_t* kv = smem + L::kKV + kvs * 2 * L::kTile;
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_rows(kv + c * kChunk, &tm_k, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh, grid.H,
+                      grid.st);
+        tma_load_rows(kv + L::kTile + c * kChunk, &tm_v, bar_kvfull + kvs, c * 64, x.j * kBlock,
+                      x.bh, grid.H, grid.st);
+      }
+      ++t;
+      return true;
+    };
+    // Q_i (+ its LSE2 and D rows) and dO_i into the next stages (lane 0).
+    auto load_q = [&](const BwdItem& x, int i) -> bool {
+      const int gq = q_issued, qs = gq % QS, ds = gq % DS;
+      if (gq >= QS && !mbar_wait(bar_qempty + qs, ((gq / QS) - 1) & 1, wd)) return false;
+      mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_rows(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
+                      i * kBlock, x.bh, grid.H, grid.st);
+      const size_t roff = static_cast<size_t>(x.bh) * Npad + static_cast<size_t>(i) * kBlock;
+      bulk_load(smem + L::kStat + qs * 1024, lse2 + roff, 512, bar_qfull + qs);
+      bulk_load(smem + L::kStat + qs * 1024 + 512, delta + roff, 512, bar_qfull + qs);
+      q_issued = gq + 1;
+      if (gq >= DS && !mbar_wait(bar_doempty + ds, ((gq / DS) - 1) & 1, wd)) return false;
+      mbar_expect_tx(bar_dofull + ds, L::kTile);
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_rows(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
+                      i * kBlock, x.bh, grid.H, grid.st);
+      do_issued = gq + 1;
+      return true;
+    };
+    if constexpr (MODE == kModeSparse) {
+      // The whole warp counts and lists the kept Q tiles window by window;
+      // lane 0 issues the copies.
       for (int r = 0; ok; ++r) {
-        const int k = bwd_item_of(grid, r);
-        if (k < 0) break;
-        const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
+        const Unit un = unit(r);
+        if (un.k < 0) break;
+        const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
         if (x.n_iter == 0) continue;
-        const int kvs = t % KVS;
-        if (t >= KVS && !mbar_wait(bar_kvempty + kvs, ((t / KVS) - 1) & 1, wd)) break;
-        mbar_expect_tx(bar_kvfull + kvs, 2 * L::kTile);
-        uint8_t* kv = smem + L::kKV + kvs * 2 * L::kTile;
-        for (int c = 0; c < L::kChunks; ++c) {
-          tma_load_rows(kv + c * kChunk, &tm_k, bar_kvfull + kvs, c * 64, x.j * kBlock, x.bh, grid.H,
-                        grid.st);
-          tma_load_rows(kv + L::kTile + c * kChunk, &tm_v, bar_kvfull + kvs, c * 64, x.j * kBlock,
-                        x.bh, grid.H, grid.st);
-        }
-        ++t;
-        for (int it = 0, i = x.i0; it < x.n_iter; ++it, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
-          const int gq = q_issued, qs = gq % QS, ds = gq % DS;
-          if (gq >= QS && !mbar_wait(bar_qempty + qs, ((gq / QS) - 1) & 1, wd)) { ok = false; break; }
-          mbar_expect_tx(bar_qfull + qs, L::kTile + 1024);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_rows(smem + L::kQ + qs * L::kTile + c * kChunk, &tm_q, bar_qfull + qs, c * 64,
-                        i * kBlock, x.bh, grid.H, grid.st);
-          const size_t roff = static_cast<size_t>(x.bh) * Npad + static_cast<size_t>(i) * kBlock;
-          bulk_load(smem + L::kStat + qs * 1024, lse2 + roff, 512, bar_qfull + qs);
-          bulk_load(smem + L::kStat + qs * 1024 + 512, delta + roff, 512, bar_qfull + qs);
-          q_issued = gq + 1;
-          if (gq >= DS && !mbar_wait(bar_doempty + ds, ((gq / DS) - 1) & 1, wd)) { ok = false; break; }
-          mbar_expect_tx(bar_dofull + ds, L::kTile);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_rows(smem + L::kDO + ds * L::kTile + c * kChunk, &tm_do, bar_dofull + ds, c * 64,
-                        i * kBlock, x.bh, grid.H, grid.st);
-          do_issued = gq + 1;
+        if (lane == 0) ok = load_kv(x);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        for (int w0 = x.ts.begin & ~127; ok && w0 < x.ts.end; w0 += 128) {
+          const int cnt = list_window(x.ts, w0, list);
+          if (lane == 0)
+            for (int idx = 0; ok && idx < cnt; ++idx) ok = load_q(x, w0 + list[idx]);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
       }
-      // Copies still in flight (only after an abort) must land before exit.
+    } else if (lane == 0) {
+      for (int r = 0; ok; ++r) {
+        const Unit un = unit(r);
+        if (un.k < 0) break;
+        const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
+        if (x.n_iter == 0) continue;
+        ok = load_kv(x);
+        for (int it = 0; ok && it < x.n_iter; ++it) ok = load_q(x, x.ts.begin + it);
+      }
+    }
+    // Copies still in flight (only after an abort) must land before exit.
+    if (lane == 0) {
       for (int u = max(0, t - KVS); u < t; ++u)
         mbar_wait_drain(bar_kvfull + (u % KVS), (u / KVS) & 1, wait_limit);
       for (int u = max(0, q_issued - QS); u < q_issued; ++u)
@@ -449,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t do_mn0 = sdesc_sw128(smem_u32(smem + L::kDO), kChunk, 1024);
       const uint64_t ds_kmaj = sdesc_sw128(smem_u32(smem + L::kDSb), 16, 1024);
       const uint64_t ds_mn = sdesc_sw128(smem_u32(smem + L::kDSb), kChunk, 1024);
-      using Cur = BwdCursor<CAUSAL, SPARSE>;
+      using Cur = BwdCursor<CAUSAL, MODE>;
       auto kv_ready = [&](const Cur& c) -> bool {
         return mbar_wait_spin_w(bar_kvfull + (c.t % KVS), (c.t / KVS) & 1, wd);
       };
@@ -478,11 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       Cur cur;
-      cur.seek(grid);
+      cur.seek(grid, unit);
       bool ok = cur.valid && kv_ready(cur) && issue_s(cur) && issue_dp(cur);
       while (ok && cur.valid) {
         Cur nx = cur;
-        nx.next(grid);
+        nx.next(grid, unit);
         const int gq = cur.g;
         const bool first = cur.it == 0, last = cur.it == cur.n - 1;
         const uint64_t q_mn = desc_adv(q_mn0, (gq % QS) * L::kTile);
@@ -557,9 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int gq = 0, t = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int k = bwd_item_of(grid, r);
-      if (k < 0) break;
-      const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
+      const Unit un = unit(r);
+      if (un.k < 0) break;
+      const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
       const int key = x.j * kBlock + row;
       const long long out_off = row_offset(grid.st, grid.H, x.bh, key);
       if (x.n_iter == 0) {  // no valid key in this tile: zero gradients
@@ -574,7 +624,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      for (int it = 0, i = x.i0; it < x.n_iter; ++it, ++gq, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
+      int w0 = (x.ts.begin & ~127) - 128, cnt = 0, idx = 0;  // window walk (block mask only)
+      for (int it = 0; it < x.n_iter; ++it, ++gq) {
+        int i = x.ts.begin + it;
+        if constexpr (MODE == kModeSparse) {
+          while (idx >= cnt) {
+            w0 += 128;
+            cnt = list_window(x.ts, w0, list);
+            idx = 0;
+          }
+          i = w0 + list[idx++];
+        }
         if (!mbar_wait_warp(bar_dqfull, gq & 1, wd)) { ok = false; break; }
         tc_fence_after();
         uint32_t v[D / 32][32];
@@ -636,7 +696,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(which == 0 ? bar_dvempty : bar_dkempty);
           }
-          if (key < N) {
+          if (MODE == kModeSplit && x.slot >= 0) {
+            // Part of a split item: fp32 into its workspace slot, column-group
+            // major ([slot][dK, dV][D / 4][128 rows][4 floats]), so that the
+            // 32 rows of a warp write 512 contiguous bytes per store.
+            float4* part = reinterpret_cast<float4*>(grid.dkv_part) +
+                           (static_cast<size_t>(x.slot) * 2 + which) * (D / 4) * kBlock + row;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+              const uint32_t* s = &a[u >> 3][(u & 7) * 4];
+              part[(h * 16 + u) * kBlock] =
+                  make_float4(__uint_as_float(s[0]) * mul, __uint_as_float(s[1]) * mul,
+                              __uint_as_float(s[2]) * mul, __uint_as_float(s[3]) * mul);
+            }
+          } else if (key < N) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               const uint32_t* s = &a[u >> 2][(u & 3) * 8];
@@ -662,12 +735,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     int gq = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int k = bwd_item_of(grid, r);
-      if (k < 0) break;
-      const BwdItem x = make_bwd_item<CAUSAL, SPARSE>(grid, k);
+      const Unit un = unit(r);
+      if (un.k < 0) break;
+      const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
       const bool key_live = x.j * kBlock + kr < x.kv_bound;
-      for (int it = 0, i = x.i0; it < x.n_iter; ++it, ++gq, i = bwd_next_row<SPARSE>(grid, x.j, i + 1)) {
-        const int s = gq % QS;  // i: the Q tile (causal diagonal, dropout draws)
+      int w0 = (x.ts.begin & ~127) - 128, cnt = 0, idx = 0;  // window walk (block mask only)
+      for (int it = 0; it < x.n_iter; ++it, ++gq) {
+        int i = x.ts.begin + it;  // the Q tile (causal diagonal, dropout draws)
+        if constexpr (MODE == kModeSparse) {
+          while (idx >= cnt) {
+            w0 += 128;
+            cnt = list_window(x.ts, w0, list);
+            idx = 0;
+          }
+          i = w0 + list[idx++];
+        }
+        const int s = gq % QS;
         const float* st_lse = reinterpret_cast<const float*>(smem + L::kStat + s * 1024) + qc0;
         const float* st_delta = st_lse + 128;
         if (!mbar_wait_warp(bar_qfull + s, (gq / QS) & 1, wd)) { ok = false; break; }
@@ -785,27 +868,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Launches the main kernel variant <D, CAUSAL, SPARSE, DROP>.
-template <int D, bool CAUSAL, bool SPARSE, bool DROP>
-cudaError_t launch_bwd_main_t(const BwdLaunch& a, cudaStream_t stream) {
+// Sums the parts of the split backward items: block s handles the key tile
+// in workspace slot s if s is the first slot holding part of it, one thread
+// per (dK or dV, key row), and writes dK = sum of the parts' dK (already
+// scaled) and dV = sum of their dV, bf16. Every part covers a different run
+// of Q tiles, so the sums are the whole accumulations
+// dK_j = scale sum_i dS_ij^T Q_i and dV_j = sum_i P_ij^T dO_i.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256) bwd_merge_kernel(BwdGrid g, __nv_bfloat16* __restrict__ dk,
+                                                        __nv_bfloat16* __restrict__ dv, int n_slots) {
+  grid_dep_wait();  // the main kernel's parts are complete
+  grid_dep_launch();
+  const int s = blockIdx.x;
+  int s_last = s;
+  if (merge_slots(g.slot_item, n_slots, s, s_last) == 0) return;
+  const int t = g.slot_item[s];
+  int bh, j;
+  bwd_item_coords(g.nt, g.BH, CAUSAL, t, bh, j);
+  const int which = threadIdx.x >> 7, rr = threadIdx.x & 127;  // which: 0 dV, 1 dK
+  float acc[D];
+#pragma unroll
+  for (int c = 0; c < D; ++c) acc[c] = 0.f;
+  for (int q = s; q <= s_last; ++q) {
+    if (g.slot_item[q] != t) continue;
+    const float4* src = reinterpret_cast<const float4*>(g.dkv_part) +
+                        (static_cast<size_t>(q) * 2 + which) * (D / 4) * kBlock + rr;
+#pragma unroll
+    for (int c = 0; c < D / 4; ++c) {
+      const float4 a = src[c * kBlock];
+      acc[4 * c] += a.x;
+      acc[4 * c + 1] += a.y;
+      acc[4 * c + 2] += a.z;
+      acc[4 * c + 3] += a.w;
+    }
+  }
+  const int key = j * kBlock + rr;
+  if (key >= g.N) return;
+  uint4* dst = reinterpret_cast<uint4*>((which ? dk : dv) + row_offset(g.st, g.H, bh, key));
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c)
+    dst[c] = make_uint4(pack_bf16(acc[8 * c], acc[8 * c + 1]), pack_bf16(acc[8 * c + 2], acc[8 * c + 3]),
+                        pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
+}
+
+// Launches bwd_main_kernel<D, CAUSAL, MODE, DROP> on `grid` CTAs (and, for
+// the split variant, the merge kernel after it).
+template <int D, bool CAUSAL, int MODE, bool DROP>
+cudaError_t launch_bwd_main_kernel(const BwdLaunch& a, const BwdGrid& g, int grid,
+                                   cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto kern = bwd_main_kernel<D, CAUSAL, SPARSE, DROP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  auto kern = bwd_main_kernel<D, CAUSAL, MODE, DROP>;
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = set_smem_once(smem_set, reinterpret_cast<const void*>(kern), L::kSmem);
   if (e != cudaSuccess) return e;
-  const int BH = a.B * a.H;
-  const int nt = (a.N + kBlock - 1) / kBlock;
-  BwdGrid g;
-  g.H = a.H;
-  g.N = a.N;
-  g.nt = nt;
-  g.BH = BH;
-  g.n_items = BH * nt;
-  g.kv_len = a.kv_len;
-  g.mask = a.block_mask;
-  g.st = a.st;
-  return launch_pdl(kern, dim3(min(g.n_items, sm_count())), dim3(kThreads), L::kSmem, stream,
-                    a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g,
-                    nt * kBlock, a.scale, a.drop, a.status, a.wait_limit);
+  e = launch_pdl(kern, dim3(grid), dim3(kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
+                 a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g, g.nt * kBlock, a.scale,
+                 a.drop, a.status, a.wait_limit);
+  if (e != cudaSuccess || MODE != kModeSplit) return e;
+  return launch_pdl(bwd_merge_kernel<D, CAUSAL>, dim3(2 * grid), dim3(256), 0, stream, g,
+                    static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), 2 * grid);
+}
+
+// The (d, causal) variants of one mode and dropout setting.
+template <int MODE, bool DROP>
+cudaError_t launch_bwd_main_variant(const BwdLaunch& a, const BwdGrid& g, int grid,
+                                    cudaStream_t stream) {
+  const bool causal = a.causal != 0;
+  if (a.d == 64)
+    return causal ? launch_bwd_main_kernel<64, true, MODE, DROP>(a, g, grid, stream)
+                  : launch_bwd_main_kernel<64, false, MODE, DROP>(a, g, grid, stream);
+  return causal ? launch_bwd_main_kernel<128, true, MODE, DROP>(a, g, grid, stream)
+                : launch_bwd_main_kernel<128, false, MODE, DROP>(a, g, grid, stream);
 }
 
 }  // namespace

@@ -7,13 +7,9 @@
 
 namespace fa {
 
-cudaError_t launch_bwd_main_sparse(const BwdLaunch& a, cudaStream_t stream) {
-  const bool causal = a.causal != 0;
-  if (a.d == 64)
-    return causal ? launch_bwd_main_t<64, true, true, false>(a, stream)
-                  : launch_bwd_main_t<64, false, true, false>(a, stream);
-  return causal ? launch_bwd_main_t<128, true, true, false>(a, stream)
-                : launch_bwd_main_t<128, false, true, false>(a, stream);
+cudaError_t launch_bwd_main_sparse(const BwdLaunch& a, const BwdGrid& g, int grid,
+                                   cudaStream_t stream) {
+  return launch_bwd_main_variant<kModeSparse, false>(a, g, grid, stream);
 }
 
 }  // namespace fa

@@ -1,16 +1,43 @@
-// Forward pass without dropout (dense, causal, key-padded and block-sparse):
-// instantiates the fused forward kernel of fa_fwd_kernel.cuh. The dropout
-// variants are compiled in fa_fwd_dropout.cu.
+// Forward pass: plans the work of a call (which work items, whether the last
+// wave is split) and launches the variant of the fused forward kernel
+// (fa_fwd_kernel.cuh) it needs. This unit compiles the plain variants
+// without dropout; the others have units of their own (fa_fwd_dropout.cu,
+// fa_fwd_sparse.cu, fa_fwd_split.cu) so that they compile in parallel.
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
 
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
-  if (a.drop.enabled) return launch_fwd_dropout(a, stream);
-  const bool causal = a.causal != 0;
-  if (a.d == 64)
-    return causal ? launch_fwd_t<64, true, false>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
-  return causal ? launch_fwd_t<128, true, false>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
+  FwdGrid g{};
+  g.H = a.H;
+  g.N = a.N;
+  g.nqt = (a.N + kBlock - 1) / kBlock;
+  g.npairs = (g.nqt + 1) / 2;
+  g.n_items = a.B * a.H * g.npairs;
+  g.kv_len = a.kv_len;
+  g.block_mask = a.block_mask;
+  g.st = a.st;
+  const int sms = sm_count();
+  const FwdSplitWorkspace ws = fwd_split_layout(sms, a.d);
+  const bool allowed = a.split_ws != nullptr && a.split_ws_bytes >= ws.total && a.kv_len == nullptr &&
+                       a.block_mask == nullptr;
+  g.plan = plan_fwd(a.B, a.H, a.N, a.d, a.causal != 0, sms, allowed);
+  if (g.plan.whole < g.plan.n_items) {
+    uint8_t* w = static_cast<uint8_t*>(a.split_ws);
+    g.slot_item = reinterpret_cast<int*>(w + ws.slot_off);
+    g.m_part = reinterpret_cast<float*>(w + ws.m_off);
+    g.l_part = reinterpret_cast<float*>(w + ws.l_off);
+    g.o_part = reinterpret_cast<float*>(w + ws.o_off);
+    return launch_fwd_split(a, g, sms, stream);
+  }
+  const int grid = min(g.n_items, sms);
+  if (a.block_mask != nullptr) return launch_fwd_sparse(a, g, grid, stream);
+  if (a.drop.enabled) return launch_fwd_plain_dropout(a, g, grid, stream);
+  return launch_fwd_plain(a, g, grid, stream);
+}
+
+cudaError_t launch_fwd_plain(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream) {
+  return launch_fwd_variant<false, kModePlain>(a, g, grid, stream);
 }
 
 }  // namespace fa

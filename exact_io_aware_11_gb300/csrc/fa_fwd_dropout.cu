@@ -40,11 +40,9 @@ __global__ void __launch_bounds__(256) dropout_mask_kernel(DropoutParams dp, int
 
 }  // namespace
 
-cudaError_t launch_fwd_dropout(const FwdLaunch& a, cudaStream_t stream) {
-  const bool causal = a.causal != 0;
-  if (a.d == 64)
-    return causal ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
-  return causal ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, false, true>(a, stream);
+cudaError_t launch_fwd_plain_dropout(const FwdLaunch& a, const FwdGrid& g, int grid,
+                                     cudaStream_t stream) {
+  return launch_fwd_variant<true, kModePlain>(a, g, grid, stream);
 }
 
 cudaError_t launch_dropout_mask(const DropoutParams& drop, int BH, int N, uint8_t* keep,

@@ -52,6 +52,7 @@
 #include "fa_internal.h"
 #include "fa_philox.cuh"
 #include "fa_ptx.cuh"
+#include "fa_sched.cuh"
 
 namespace fa {
 namespace {
@@ -83,7 +84,7 @@ struct FwdLayout {
   static constexpr int kK = kQ + 2 * kQS * kTile;
   static constexpr int kV = kK + kKS * kTile;
   static constexpr int kBar = kV + kVS * kTile;
-  static constexpr int kEnd = kBar + 256;
+  static constexpr int kEnd = kBar + 512 + 8 * 128;  // barriers, TMEM address, abort flag, tail range; tile lists
   static constexpr int kSmem = kEnd + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t kTO = 256;       // O_A; O_B at kTO + D
   // P_t (bf16 pairs, 64 columns): its own columns, or over the first 64 of S_t
@@ -117,73 +118,62 @@ __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// Which K/V tiles a Q tile visits: j < end, and the block-mask bit if any.
-struct TileSet {
-  int end;
-  const uint8_t* mrow;
-  __device__ bool has(int j) const { return j < end && (mrow == nullptr || mrow[j] != 0); }
-  __device__ int last() const {  // last visited tile, -1 if none
-    int j = end - 1;
-    if (mrow != nullptr)
-      while (j >= 0 && mrow[j] == 0) --j;
-    return j;
-  }
-};
-
-// One work item: Q tiles 2p and 2p+1 (B = -1 if absent) of one (batch, head).
+// One work unit: Q tiles 2p and 2p+1 (qtB = -1 if absent) of one (batch,
+// head), restricted to the K/V steps [sb, se) of the unit. Without a block
+// mask or key padding, step j is K/V tile j, so a unit of a split item covers
+// K/V tiles [sb, se); `slot` >= 0 names the workspace slot its partial result
+// goes to (-1: the whole item, O and LSE written directly).
 struct FwdItem {
-  int bh, qtA, qtB, kv_bound, uend;
+  int k, bh, qtA, qtB, kv_bound, slot;
   TileSet tsA, tsB;
 };
 
-struct FwdGrid {
-  int H, N, nqt, npairs, n_items;
-  Strides st;  // of q, k, v, o
-  const int32_t* kv_len;
-  const uint8_t* block_mask;
-};
-
-// Item k. Causal items are ordered heaviest first (pairs near the diagonal end
-// see the most K/V tiles); otherwise a head's pairs are consecutive.
 template <bool CAUSAL>
-__device__ FwdItem make_item(const FwdGrid& g, int k) {
+__host__ __device__ __forceinline__ int fwd_steps(const FwdGrid& g, int k) {
+  return fwd_item_steps(g.nqt, g.npairs, g.n_items / g.npairs, CAUSAL, k);
+}
+
+template <bool CAUSAL>
+__device__ FwdItem make_item(const FwdGrid& g, const Unit& u) {
   FwdItem it;
-  const int BH = g.n_items / g.npairs;
   int p;
-  if (CAUSAL) {
-    p = g.npairs - 1 - k / BH;
-    it.bh = k % BH;
-  } else {
-    it.bh = k / g.npairs;
-    p = k % g.npairs;
-  }
+  fwd_item_coords(g.npairs, g.n_items / g.npairs, CAUSAL, u.k, it.bh, p);
+  it.k = u.k;
+  it.slot = u.slot;
   it.qtA = 2 * p;
   it.qtB = 2 * p + 1 < g.nqt ? 2 * p + 1 : -1;
   it.kv_bound = g.N;
   if (g.kv_len != nullptr) it.kv_bound = min(g.N, max(0, g.kv_len[it.bh / g.H]));
   const int kv_tiles = (it.kv_bound + kBlock - 1) / kBlock;
-  it.tsA.end = CAUSAL ? min(kv_tiles, it.qtA + 1) : kv_tiles;
-  it.tsA.mrow = g.block_mask != nullptr ? g.block_mask + static_cast<size_t>(it.qtA) * g.nqt : nullptr;
-  it.tsB.end = it.qtB < 0 ? 0 : (CAUSAL ? min(kv_tiles, it.qtB + 1) : kv_tiles);
-  it.tsB.mrow = (g.block_mask != nullptr && it.qtB >= 0)
-                    ? g.block_mask + static_cast<size_t>(it.qtB) * g.nqt
-                    : nullptr;
-  it.uend = max(it.tsA.end, it.tsB.end);
+  const int endA = CAUSAL ? min(kv_tiles, it.qtA + 1) : kv_tiles;
+  const int endB = it.qtB < 0 ? 0 : (CAUSAL ? min(kv_tiles, it.qtB + 1) : kv_tiles);
+  const uint8_t* mA = g.block_mask != nullptr ? g.block_mask + static_cast<size_t>(it.qtA) * g.nqt : nullptr;
+  const uint8_t* mB = (g.block_mask != nullptr && it.qtB >= 0)
+                          ? g.block_mask + static_cast<size_t>(it.qtB) * g.nqt
+                          : nullptr;
+  it.tsA = TileSet{u.sb, min(endA, u.se), mA, 1};
+  it.tsB = TileSet{u.sb, min(endB, u.se), mB, 1};
   return it;
 }
 
-// The r-th item of this CTA: a snake over the (heaviest-first) item list, so
-// that every CTA gets a similar amount of work; -1 when there is none.
-__device__ __forceinline__ int item_of(const FwdGrid& g, int r) {
-  const int G = gridDim.x, c = blockIdx.x;
-  if (r * G >= g.n_items) return -1;
-  const int k = r * G + ((r & 1) ? G - 1 - c : c);
-  return k < g.n_items ? k : -1;  // only the last round can run past the end
+// The next K/V tile >= j that Q tile A or B of an item visits (kNoTile if
+// none), and which of the two visit it. Warp-collective.
+__device__ __forceinline__ int next_pair_tile(TileWalk<>& wa, TileWalk<>& wb, int j, bool& hA, bool& hB) {
+  const int a = wa.seek(j), b = wb.seek(j);
+  const int m = min(a, b);
+  hA = a == m;
+  hB = b == m;
+  return m;
 }
 
 // DROP: inverted dropout on P (fa_philox.cuh); the row sums and LSE use the
 // undropped P, the PV product the dropped one, and O is scaled by 1 / (1 - p').
-template <int D, bool CAUSAL, bool DROP>
+// MODE (kModePlain, kModeSparse, kModeSplit): the variant compiled. Plain
+// walks dense ranges of K/V tiles and whole items; sparse walks the tile
+// lists of a block mask; split also runs the parts of the last wave's items
+// and writes their partial results. Keeping them apart at compile time leaves
+// the plain kernel's hot loops exactly as tuned.
+template <int D, bool CAUSAL, bool DROP, int MODE>
 __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
@@ -208,6 +198,8 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   uint64_t* bar_final = bars + 28;   // [2] one per MMA issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
   int* abort_flag = reinterpret_cast<int*>(bars + 31);
+  TailRange* tail_sh = reinterpret_cast<TailRange*>(bars + 32);  // this CTA's share of a split tail
+  uint8_t* walk_list = reinterpret_cast<uint8_t*>(bars + 64);     // [warp][128] kept tiles of a window (sparse)
   constexpr int kMmaB = FwdWarps<D>::kMmaB, kSoft0 = FwdWarps<D>::kSoft0;
   constexpr int kIssuers = kSepP ? 2 : 1;  // arrivals that release a K or V ring slot
 
@@ -242,6 +234,13 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  auto steps = [&](int k) { return fwd_steps<CAUSAL>(g, k); };
+  if constexpr (MODE == kModeSplit) {
+    if (warp == kLoadWarp) {
+      const TailRange tr = tail_range(g.plan, blockIdx.x, gridDim.x, steps);
+      if (lane == 0) *tail_sh = tr;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -249,52 +248,112 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
   grid_dep_launch();
   const Watchdog wd{wait_limit, status, abort_flag};
+  if constexpr (MODE == kModeSplit) {
+    if (threadIdx.x == 0) {
+      const TailRange tr = *tail_sh;
+      write_slot_items(g.slot_item, tr, blockIdx.x, tr.t1 >= tr.t0 ? steps(tr.t0) : 0,
+                       tr.t1 >= tr.t0 ? steps(tr.t1) : 0);
+    }
+  }
+  // The r-th unit of this CTA, or a unit with k < 0: whole items in a snake
+  // over the item list, and for a split plan the parts of its tail.
+  auto unit = [&](int r) -> Unit {
+    if constexpr (MODE == kModeSplit) {
+      return unit_of(g.plan, tail_sh, r, blockIdx.x, gridDim.x, steps);
+    } else {
+      Unit u{-1, 0, 1 << 30, -1};
+      const int G = gridDim.x, c = blockIdx.x;
+      if (r * G >= g.n_items) return u;
+      const int k = r * G + ((r & 1) ? G - 1 - c : c);
+      if (k < g.n_items) u.k = k;  // only the last round can run past the end
+      return u;
+    }
+  };
+  uint8_t* list = walk_list + 128 * warp;
 
   if (warp == kLoadWarp) {
-    // ------------------------------------------------------------ TMA producer (one lane)
+    // ------------------------------------------------------------ TMA producer
+    // Lane 0 waits for free ring slots and issues the copies (with a block
+    // mask the whole warp first lists each window's tiles).
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      int nqA = 0, nqB = 0;  // Q loads issued per slot
-      int k_issued = 0, v_issued = 0;
-      int u = 0;           // position in the K/V rings, continued across items
-      bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int k = item_of(g, r);
-        if (k < 0) break;
-        const FwdItem it = make_item<CAUSAL>(g, k);
+    }
+    int nqA = 0, nqB = 0;  // Q loads issued per slot
+    int k_issued = 0, v_issued = 0;
+    int u = 0;           // position in the K/V rings, continued across items
+    bool ok = true;
+    // Q loads of a unit's two tiles (lane 0); false on an abort.
+    auto load_q = [&](const FwdItem& it, int lastA, int lastB) -> bool {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if ((t ? it.tsB : it.tsA).last() < 0) continue;
-          int& nq = t ? nqB : nqA;
-          const int qb = t * QS + nq % QS;
-          if (nq >= QS && !mbar_wait(bar_qempty + qb, ((nq / QS) - 1) & 1, wd)) { ok = false; break; }
-          mbar_expect_tx(bar_qfull + qb, L::kTile);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_rows(smem + L::kQ + qb * L::kTile + c * kChunk, &tm_q, bar_qfull + qb, c * 64,
+      for (int t = 0; t < 2; ++t) {
+        if ((t ? lastB : lastA) < 0) continue;
+        int& nq = t ? nqB : nqA;
+        const int qb = t * QS + nq % QS;
+        if (nq >= QS && !mbar_wait(bar_qempty + qb, ((nq / QS) - 1) & 1, wd)) return false;
+        mbar_expect_tx(bar_qfull + qb, L::kTile);
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_rows(smem + L::kQ + qb * L::kTile + c * kChunk, &tm_q, bar_qfull + qb, c * 64,
                         (t ? it.qtB : it.qtA) * kBlock, it.bh, g.H, g.st);
-          ++nq;
-        }
-        for (int j = 0; ok && j < it.uend; ++j) {
-          if (!it.tsA.has(j) && !it.tsB.has(j)) continue;
-          const int ks = u % KS, vs = u % VS;
-          if (u >= KS && !mbar_wait(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) { ok = false; break; }
-          mbar_expect_tx(bar_kfull + ks, L::kTile);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_rows(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
-                        j * kBlock, it.bh, g.H, g.st);
-          k_issued = u + 1;
-          if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) { ok = false; break; }
-          mbar_expect_tx(bar_vfull + vs, L::kTile);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_rows(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
-                        j * kBlock, it.bh, g.H, g.st);
-          v_issued = u + 1;
-          ++u;
+        ++nq;
+      }
+      return true;
+    };
+    // K_j and V_j into the next ring position (lane 0); false on an abort.
+    auto load_kv = [&](const FwdItem& it, int j) -> bool {
+      const int ks = u % KS, vs = u % VS;
+      if (u >= KS && !mbar_wait(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) return false;
+      mbar_expect_tx(bar_kfull + ks, L::kTile);
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_rows(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
+                      j * kBlock, it.bh, g.H, g.st);
+      k_issued = u + 1;
+      if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) return false;
+      mbar_expect_tx(bar_vfull + vs, L::kTile);
+      for (int c = 0; c < L::kChunks; ++c)
+        tma_load_rows(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
+                      j * kBlock, it.bh, g.H, g.st);
+      v_issued = u + 1;
+      ++u;
+      return true;
+    };
+    if constexpr (MODE == kModeSparse) {
+      // The whole warp lists each 128-tile window's tiles (union of the two Q
+      // tiles' mask rows); lane 0 then issues their copies.
+      for (int r = 0; ok; ++r) {
+        const Unit un = unit(r);
+        if (un.k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, un);
+        TileWalk<> wa, wb;
+        wa.init(it.tsA);
+        wb.init(it.tsB);
+        const int lastA = wa.last(), lastB = wb.last();
+        if (lane == 0) ok = load_q(it, lastA, lastB);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        const int uend = max(it.tsA.end, it.tsB.end);
+        for (int w0 = it.tsA.begin & ~127; ok && w0 < uend; w0 += 128) {
+          const int cnt = list_window2(it.tsA, it.tsB, w0, list);
+          if (lane == 0)
+            for (int idx = 0; ok && idx < cnt; ++idx) ok = load_kv(it, w0 + list[idx]);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
       }
-      // Let every copy in flight land before the CTA can exit (bounded).
+    } else if (lane == 0) {
+      // Dense ranges: K/V tiles [begin, max(end_A, end_B)) of every unit.
+      for (int r = 0; ok; ++r) {
+        const Unit un = unit(r);
+        if (un.k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, un);
+        const int lastA = it.tsA.end > it.tsA.begin ? it.tsA.end - 1 : -1;
+        const int lastB = it.tsB.end > it.tsB.begin ? it.tsB.end - 1 : -1;
+        ok = load_q(it, lastA, lastB);
+        const int uend = max(it.tsA.end, it.tsB.end);
+        for (int j = it.tsA.begin; ok && j < uend; ++j) ok = load_kv(it, j);
+      }
+    }
+    // Let every copy in flight land before the CTA can exit (bounded).
+    if (lane == 0) {
       for (int t = 0; t < 2; ++t) {
         const int nq = t ? nqB : nqA;
         for (int q = max(0, nq - QS); q < nq; ++q)
@@ -347,11 +406,30 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         return true;
       };
       for (int r = 0; ok; ++r) {
-        const int k = item_of(g, r);
-        if (k < 0) break;
-        const FwdItem it = make_item<CAUSAL>(g, k);
-        const TileSet my = X ? it.tsB : it.tsA;
-        const int last = my.last();
+        const Unit un0 = unit(r);
+        if (un0.k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, un0);
+        TileWalk<> wa, wb;  // block-mask walks (sparse)
+        wa.init(it.tsA);
+        wb.init(it.tsB);
+        const int uend = max(it.tsA.end, it.tsB.end);
+        // The next K/V tile >= j of the item and whether Q tiles A, B visit it.
+        auto nxt = [&](int j, bool& hA, bool& hB) -> int {
+          if constexpr (MODE == kModeSparse) {
+            return next_pair_tile(wa, wb, j, hA, hB);
+          } else {
+            hA = j < it.tsA.end;
+            hB = j < it.tsB.end;
+            return j < uend ? j : kNoTile;
+          }
+        };
+        int last;  // the last K/V tile Q tile X visits (-1: none)
+        if constexpr (MODE == kModeSparse) {
+          last = X ? wb.last() : wa.last();
+        } else {
+          const TileSet& my = X ? it.tsB : it.tsA;
+          last = my.end > my.begin ? my.end - 1 : -1;
+        }
         bool needq = last >= 0;
         int loc = 0;  // P V MMAs of this item
         const int qb = X * QS + nq % QS;
@@ -412,30 +490,32 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           mbar_arrive_w(bar_vempty + (uu % VS));
           return true;
         };
-        int j = 0;
-        while (j < it.uend && !it.tsA.has(j) && !it.tsB.has(j)) ++j;
-        if (j >= it.uend) continue;
+        bool jA, jB;
+        int j = nxt(it.tsA.begin, jA, jB);
+        if (j == kNoTile) continue;
         {
-          const bool h = my.has(j);
+          const bool h = X ? jB : jA;
           if (h) ok = issue_s(u, j);
           if (ok) ok = release_k(u, h);
         }
-        while (ok && j < it.uend) {
-          int jn = j + 1;
-          while (jn < it.uend && !it.tsA.has(jn) && !it.tsB.has(jn)) ++jn;
+        while (ok && j != kNoTile) {
+          bool nA, nB;
+          const int jn = nxt(j + 1, nA, nB);
           const int un = u + 1;
           // S_X(j+1) as soon as the softmax has read S_X(j), then P_X(j) V_j
-          if (jn < it.uend) {
-            const bool h = my.has(jn);
+          if (jn != kNoTile) {
+            const bool h = X ? nB : nA;
             if (h) ok = issue_s(un, jn);
             if (ok) ok = release_k(un, h);
           }
           if (ok) {
-            const bool h = my.has(j);
+            const bool h = X ? jB : jA;
             if (h) ok = issue_pv(u);
             if (ok) ok = release_v(u, h);
           }
           j = jn;
+          jA = nA;
+          jB = nB;
           u = un;
         }
       }
@@ -459,10 +539,30 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       using SlotA = std::integral_constant<int, 0>;
       using SlotB = std::integral_constant<int, 1>;
       for (int r = 0; ok; ++r) {
-        const int k = item_of(g, r);
-        if (k < 0) break;
-        const FwdItem it = make_item<CAUSAL>(g, k);
-        const int lastA = it.tsA.last(), lastB = it.tsB.last();
+        const Unit un0 = unit(r);
+        if (un0.k < 0) break;
+        const FwdItem it = make_item<CAUSAL>(g, un0);
+        TileWalk<> wa, wb;  // block-mask walks (sparse)
+        wa.init(it.tsA);
+        wb.init(it.tsB);
+        const int uend = max(it.tsA.end, it.tsB.end);
+        auto nxt = [&](int j, bool& hA, bool& hB) -> int {
+          if constexpr (MODE == kModeSparse) {
+            return next_pair_tile(wa, wb, j, hA, hB);
+          } else {
+            hA = j < it.tsA.end;
+            hB = j < it.tsB.end;
+            return j < uend ? j : kNoTile;
+          }
+        };
+        int lastA, lastB;
+        if constexpr (MODE == kModeSparse) {
+          lastA = wa.last();
+          lastB = wb.last();
+        } else {
+          lastA = it.tsA.end > it.tsA.begin ? it.tsA.end - 1 : -1;
+          lastB = it.tsB.end > it.tsB.begin ? it.tsB.end - 1 : -1;
+        }
         bool needqA = lastA >= 0, needqB = lastB >= 0;
         int locA = 0, locB = 0;  // P V MMAs of this item per slot
         auto issue_s = [&](auto slot, int uu, int j) -> bool {
@@ -515,37 +615,40 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           ++loc;
           return true;
         };
-        int j = 0;
-        while (j < it.uend && !it.tsA.has(j) && !it.tsB.has(j)) ++j;
-        if (j >= it.uend) continue;
-        if (it.tsA.has(j)) ok = issue_s(SlotA{}, u, j);
-        if (ok && it.tsB.has(j)) ok = issue_s(SlotB{}, u, j);
+        bool jA, jB;
+        int j = nxt(it.tsA.begin, jA, jB);
+        if (j == kNoTile) continue;
+        if (jA) ok = issue_s(SlotA{}, u, j);
+        if (ok && jB) ok = issue_s(SlotB{}, u, j);
         if (ok) mma_commit_w(bar_kempty + (u % KS));
-        while (ok && j < it.uend) {
-          int jn = j + 1;
-          while (jn < it.uend && !it.tsA.has(jn) && !it.tsB.has(jn)) ++jn;
+        while (ok && j != kNoTile) {
+          bool nA, nB;
+          const int jn = nxt(j + 1, nA, nB);
+          const bool more = jn != kNoTile;
           const int un = u + 1;
           if constexpr (kSepP) {
             // S_t(j+1) as soon as the softmax has read S_t(j), so that it is
             // ready when P_t(j) is; then P_A(j) V_j and P_B(j) V_j.
-            if (jn < it.uend) {
-              if (it.tsA.has(jn)) ok = issue_s(SlotA{}, un, jn);
-              if (ok && it.tsB.has(jn)) ok = issue_s(SlotB{}, un, jn);
+            if (more) {
+              if (nA) ok = issue_s(SlotA{}, un, jn);
+              if (ok && nB) ok = issue_s(SlotB{}, un, jn);
               if (ok) mma_commit_w(bar_kempty + (un % KS));
             }
-            if (ok && it.tsA.has(j)) ok = issue_pv(SlotA{}, u);
-            if (ok && it.tsB.has(j)) ok = issue_pv(SlotB{}, u);
+            if (ok && jA) ok = issue_pv(SlotA{}, u);
+            if (ok && jB) ok = issue_pv(SlotB{}, u);
             if (ok) mma_commit_w(bar_vempty + (u % VS));
           } else {
             // tile A: P_A(j) V_j, then S_A(j+1) over the columns P_A(j) just left
-            if (it.tsA.has(j)) ok = issue_pv(SlotA{}, u);
-            if (ok && jn < it.uend && it.tsA.has(jn)) ok = issue_s(SlotA{}, un, jn);
-            if (ok && it.tsB.has(j)) ok = issue_pv(SlotB{}, u);
+            if (jA) ok = issue_pv(SlotA{}, u);
+            if (ok && more && nA) ok = issue_s(SlotA{}, un, jn);
+            if (ok && jB) ok = issue_pv(SlotB{}, u);
             if (ok) mma_commit_w(bar_vempty + (u % VS));
-            if (ok && jn < it.uend && it.tsB.has(jn)) ok = issue_s(SlotB{}, un, jn);
-            if (ok && jn < it.uend) mma_commit_w(bar_kempty + (un % KS));
+            if (ok && more && nB) ok = issue_s(SlotB{}, un, jn);
+            if (ok && more) mma_commit_w(bar_kempty + (un % KS));
           }
           j = jn;
+          jA = nA;
+          jB = nB;
           u = un;
         }
       }
@@ -564,22 +667,22 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     int ns = 0;  // S tiles of this slot consumed so far (sfull / pfull / odone phases)
     bool ok = true;
     for (int ri = 0; ok; ++ri) {
-      const int k = item_of(g, ri);
-      if (k < 0) break;
-      const FwdItem it = make_item<CAUSAL>(g, k);
+      const Unit un0 = unit(ri);
+      if (un0.k < 0) break;
+      const FwdItem it = make_item<CAUSAL>(g, un0);
       const int qt = t ? it.qtB : it.qtA;
       if (qt < 0) continue;
-      const TileSet my = t ? it.tsB : it.tsA;
+      const int jbeg = t ? it.tsB.begin : it.tsA.begin, jend = t ? it.tsB.end : it.tsA.end;
       const int kv_bound = it.kv_bound;
       const int row = qt * kBlock + r;
       float m = -INFINITY;  // reference max, log2 units (scale folded in)
       float l = 0.f;        // sum of exp2(s * scale_log2 - m) over visited keys
       int n = 0;            // tiles of this item
-      for (int j = 0; j < my.end; ++j) {
-        if (!my.has(j)) continue;
+      // One K/V tile j of this slot: S_t(j) from TMEM, the online softmax
+      // update, P_t(j) to TMEM, then pfull. False when the CTA is aborting.
+      auto tile = [&](const int j) -> bool {
         if (!mbar_wait_warp<true>(bar_sfull + t, ns & 1, wd)) {
-          ok = false;
-          break;
+          return false;
         }
         tc_fence_after();
         uint32_t rs[4][32];
@@ -622,8 +725,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         if (kSepP && n >= 1) {
           // P_t's columns are free (and O quiescent) once this item's previous P V is done.
           if (!mbar_wait_warp<true>(bar_odone + t, (ns - 1) & 1, wd)) {
-            ok = false;
-            break;
+            return false;
           }
           tc_fence_after();
         }
@@ -661,8 +763,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           // O must be quiescent (this item's previous P V done) before it is rescaled.
           if (!kSepP) {
             if (!mbar_wait_warp<true>(bar_odone + t, (ns - 1) & 1, wd)) {
-              ok = false;
-              break;
+              return false;
             }
             tc_fence_after();
           }
@@ -685,6 +786,19 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         if (lane == 0) mbar_arrive(bar_pfull + t);
         ++n;
         ++ns;
+        return true;
+      };
+      if constexpr (MODE == kModeSparse) {
+        // Window by window (128 tiles): the mask row's kept tiles are listed
+        // in the warp's shared-memory list first.
+        for (int w0 = jbeg & ~127; ok && w0 < jend; w0 += 128) {
+          const int cnt =
+              list_window(TileSet{jbeg, jend, g.block_mask + static_cast<size_t>(qt) * g.nqt, 1}, w0, list);
+          for (int idx = 0; ok && idx < cnt; ++idx) ok = tile(w0 + list[idx]);
+          __syncwarp();  // the list may be rewritten for the next window
+        }
+      } else {
+        for (int j = jbeg; ok && j < jend; ++j) ok = tile(j);
       }
       if (!ok) break;
       // ---------------------------------------------------------- epilogue
@@ -698,6 +812,33 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           break;
         }
         tc_fence_after();
+      }
+      if (MODE == kModeSplit && it.slot >= 0) {
+        // Part of a split item: the unnormalised O, the row's running maximum
+        // and sum go to the item's workspace slot; the merge kernel combines
+        // the parts into O and LSE.
+        // O is stored column-group major ([slot][D / 4][256 rows][4 floats]),
+        // so that the 32 rows of a warp write 512 contiguous bytes per store.
+        const size_t prow = static_cast<size_t>(it.slot) * 256 + t * kBlock + r;
+        g.m_part[prow] = m;
+        g.l_part[prow] = l;
+        if (have) {
+          float4* dst = reinterpret_cast<float4*>(g.o_part) + static_cast<size_t>(it.slot) * (D / 4) * 256 +
+                        t * kBlock + r;
+#pragma unroll
+          for (int c0 = 0; c0 < D / 32; ++c0) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + o_col + c0 * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[(c0 * 8 + v) * 256] =
+                  make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                              __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+          }
+        }
+        continue;
       }
       const bool live = have && l > 0.f;
       const float inv = live ? (DROP ? dp.rescale : 1.f) / l : 0.f;
@@ -739,25 +880,93 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool DROP>
-cudaError_t launch_fwd_t(const FwdLaunch& a, cudaStream_t stream) {
+// Merges the parts of the split items. Block s handles the item in
+// workspace slot s if s is the first slot that holds part of it, one thread
+// per row of its two Q tiles: with m_q, l_q, O_q the running maximum (log2
+// units), sum and unnormalised output of part q of the row, M = max_q m_q and
+//   O = r sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q,
+//   LSE = (M + log2 sum_q 2^(m_q - M) l_q) ln 2,
+// which is the online-softmax rescaling applied once more, across the parts
+// (r = 1 / (1 - p') with dropout, else 1). Parts that saw no key (l = 0) do
+// not contribute; a row with no part left gets O = 0 and LSE = -inf. The
+// partial O is read column-group major, 512 contiguous bytes per warp load.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256) fwd_merge_kernel(FwdGrid g, __nv_bfloat16* __restrict__ out,
+                                                        float* __restrict__ lse_out, int n_slots,
+                                                        float rescale) {
+  grid_dep_wait();  // the main kernel's parts are complete
+  grid_dep_launch();
+  const int s = blockIdx.x;
+  int s_last = s;
+  if (merge_slots(g.slot_item, n_slots, s, s_last) == 0) return;
+  const int t = g.slot_item[s];
+  int bh, p;
+  fwd_item_coords(g.npairs, g.n_items / g.npairs, CAUSAL, t, bh, p);
+  const int x = threadIdx.x;  // row of the pair: tile x / 128, row x % 128
+  const int qt = 2 * p + (x >> 7), row = qt * kBlock + (x & 127);
+  float M = -INFINITY;
+  for (int q = s; q <= s_last; ++q)
+    if (g.slot_item[q] == t && g.l_part[static_cast<size_t>(q) * 256 + x] > 0.f)
+      M = fmaxf(M, g.m_part[static_cast<size_t>(q) * 256 + x]);
+  float Lsum = 0.f;
+  float acc[D];
+#pragma unroll
+  for (int c = 0; c < D; ++c) acc[c] = 0.f;
+  for (int q = s; q <= s_last; ++q) {
+    if (g.slot_item[q] != t) continue;
+    const float l = g.l_part[static_cast<size_t>(q) * 256 + x];
+    if (!(l > 0.f)) continue;
+    const float w = exp2f(g.m_part[static_cast<size_t>(q) * 256 + x] - M);
+    Lsum += w * l;
+    const float4* src = reinterpret_cast<const float4*>(g.o_part) + static_cast<size_t>(q) * (D / 4) * 256 + x;
+#pragma unroll
+    for (int c = 0; c < D / 4; ++c) {
+      const float4 a = src[c * 256];
+      acc[4 * c] += w * a.x;
+      acc[4 * c + 1] += w * a.y;
+      acc[4 * c + 2] += w * a.z;
+      acc[4 * c + 3] += w * a.w;
+    }
+  }
+  if (qt >= g.nqt || row >= g.N) return;
+  lse_out[static_cast<size_t>(bh) * g.N + row] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+  const float inv = Lsum > 0.f ? rescale / Lsum : 0.f;
+  uint4* dst = reinterpret_cast<uint4*>(out + row_offset(g.st, g.H, bh, row));
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c)
+    dst[c] = make_uint4(pack_bf16(acc[8 * c] * inv, acc[8 * c + 1] * inv),
+                        pack_bf16(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
+                        pack_bf16(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv),
+                        pack_bf16(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
+}
+
+// Launches fwd_kernel<D, CAUSAL, DROP, MODE> on `grid` CTAs (and, for the
+// split variant, the merge kernel after it).
+template <int D, bool CAUSAL, bool DROP, int MODE>
+cudaError_t launch_fwd_kernel(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, CAUSAL, DROP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  auto kern = fwd_kernel<D, CAUSAL, DROP, MODE>;
+  static std::atomic<unsigned long long> smem_set{0};
+  cudaError_t e = set_smem_once(smem_set, reinterpret_cast<const void*>(kern), L::kSmem);
   if (e != cudaSuccess) return e;
-  FwdGrid g;
-  g.H = a.H;
-  g.N = a.N;
-  g.nqt = (a.N + kBlock - 1) / kBlock;
-  g.npairs = (g.nqt + 1) / 2;
-  g.n_items = a.B * a.H * g.npairs;
-  g.kv_len = a.kv_len;
-  g.block_mask = a.block_mask;
-  g.st = a.st;
-  const int grid = min(g.n_items, sm_count());
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  return launch_pdl(kern, dim3(grid), dim3(FwdWarps<D>::kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
-                    a.o, a.lse, g, scale_log2, a.drop, a.status, a.wait_limit);
+  e = launch_pdl(kern, dim3(grid), dim3(FwdWarps<D>::kThreads), L::kSmem, stream, a.tm_q, a.tm_k,
+                 a.tm_v, a.o, a.lse, g, scale_log2, a.drop, a.status, a.wait_limit);
+  if (e != cudaSuccess || MODE != kModeSplit) return e;
+  return launch_pdl(fwd_merge_kernel<D, CAUSAL>, dim3(2 * grid), dim3(256), 0, stream, g,
+                    static_cast<__nv_bfloat16*>(a.o), a.lse, 2 * grid,
+                    a.drop.enabled ? a.drop.rescale : 1.f);
+}
+
+// The (d, causal) variants of one dropout setting and mode.
+template <bool DROP, int MODE>
+cudaError_t launch_fwd_variant(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream) {
+  const bool causal = a.causal != 0;
+  if (a.d == 64)
+    return causal ? launch_fwd_kernel<64, true, DROP, MODE>(a, g, grid, stream)
+                  : launch_fwd_kernel<64, false, DROP, MODE>(a, g, grid, stream);
+  return causal ? launch_fwd_kernel<128, true, DROP, MODE>(a, g, grid, stream)
+                : launch_fwd_kernel<128, false, DROP, MODE>(a, g, grid, stream);
 }
 
 }  // namespace

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 
@@ -44,6 +45,31 @@ __host__ __device__ __forceinline__ long long row_offset(const Strides& s, int H
          static_cast<long long>(n) * s.n;
 }
 
+// How a persistent kernel's work items are shared out over its G CTAs
+// (fa_sched.cuh). Items [0, whole) are handed out whole, round r to CTA
+// (r odd ? G-1-c : c) of item r G + c (a snake over an item list ordered
+// heaviest first, so that CTAs get similar totals). When whole < n_items the
+// items [whole, n_items) form the tail: they are laid end to end as steps and
+// CTAs 0 .. tail_ctas - 1 take equal runs of them; whole is then a multiple
+// of G. When whole == n_items nothing is split and the last round may be short.
+struct SplitPlan {
+  int n_items;
+  int whole;
+  long long tail;  // steps of the tail items
+  int tail_ctas;
+};
+
+// The part of the tail one CTA runs: steps o0.. of item t0 up to (but not
+// including) step o1 of item t1; no tail work when t1 < t0.
+struct TailRange {
+  int t0, o0, t1, o1;
+};
+
+// Compile-time variants of the persistent kernels: plain (whole items, dense
+// tile ranges), sparse (tile lists from a block mask) and split (the last wave
+// cut into parts whose partial results a merge kernel combines).
+constexpr int kModePlain = 0, kModeSparse = 1, kModeSplit = 2;
+
 // Dropout on the attention probabilities (inverted: kept entries are scaled
 // by 1 / (1 - p')). Element (b, h, i, j) draws byte j mod 16 of the
 // Philox4x32-10 block at counter (j / 16, i, b*H + h, offset) under key
@@ -56,8 +82,82 @@ struct DropoutParams {
   int enabled;        // 0: no dropout (the other fields are ignored)
 };
 
+// Workspace of a split forward (see fa_sched.cuh): per CTA two slots, each
+// holding one partial result of a pair of Q tiles -- the tail item it belongs
+// to, and per row the running maximum, the running sum and the unnormalised
+// O (fp32). Regions are 256-byte aligned.
+struct FwdSplitWorkspace {
+  size_t slot_off, m_off, l_off, o_off, total;
+};
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline FwdSplitWorkspace fwd_split_layout(int G, int d) {
+  FwdSplitWorkspace w{};
+  const size_t slots = 2 * static_cast<size_t>(G);
+  w.slot_off = 0;
+  w.m_off = align256(slots * 4);
+  w.l_off = w.m_off + align256(slots * 256 * 4);
+  w.o_off = w.l_off + align256(slots * 256 * 4);
+  w.total = w.o_off + align256(slots * 256 * static_cast<size_t>(d) * 4);
+  return w;
+}
+
+// Extra workspace of a split backward, placed after the regions of
+// BwdWorkspace: per slot the tail item it holds and a partial dK, dV (fp32,
+// 128 key rows x d each, dK already multiplied by the scale).
+struct BwdSplitWorkspace {
+  size_t slot_off, dkv_off, total;  // offsets from the start of the split area
+};
+inline BwdSplitWorkspace bwd_split_layout(int G, int d) {
+  BwdSplitWorkspace w{};
+  const size_t slots = 2 * static_cast<size_t>(G);
+  w.slot_off = 0;
+  w.dkv_off = align256(slots * 4);
+  w.total = w.dkv_off + align256(slots * 2 * 128 * static_cast<size_t>(d) * 4);
+  return w;
+}
+
+// Sets a kernel's dynamic shared-memory limit once per device: `done` holds
+// one bit per device ordinal (a static of the caller, one per kernel).
+inline cudaError_t set_smem_once(std::atomic<unsigned long long>& done, const void* kern, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0ull && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0ull) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
+// Forward work: items are pairs of 128-row Q tiles of one (batch, head).
+struct FwdGrid {
+  int H, N, nqt, npairs, n_items;
+  Strides st;  // of q, k, v, o
+  const int32_t* kv_len;
+  const uint8_t* block_mask;
+  SplitPlan plan;
+  // split plans only: workspace slots of the partial results
+  int* slot_item;  // [2G] tail item held by each slot, or -1
+  float* m_part;   // [2G][256] running maximum (log2 units) of each row
+  float* l_part;   // [2G][256] running sum of each row
+  float* o_part;   // [2G][d / 4][256][4] unnormalised O, column-group major
+};
+
+// Backward work: items are 128-key tiles of one (batch, head).
+struct BwdGrid {
+  int H, N, nt, BH, n_items;
+  Strides st;  // of q, k, v, dout, dk, dv
+  const int32_t* kv_len;
+  const uint8_t* mask;  // block-sparse: uint8 [nt][nt], nonzero = (query tile, key tile) kept
+  SplitPlan plan;
+  int* slot_item;   // split plans: [2G] tail item held by each slot, or -1
+  float* dkv_part;  // split plans: [2G][2][d / 4][128][4] partial dV, dK (x scale)
+};
+
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps (d, N, H, B) with the call's strides, box 64 x 128 x 1 x 1, 128B swizzle
+  void* split_ws;         // workspace for a split of the last wave, or nullptr
+  size_t split_ws_bytes;
   void* o;
   float* lse;
   int B, H, N, d;
@@ -89,6 +189,8 @@ struct BwdLaunch {
   float* lse2;     // workspace: fp32 [B*H, Npad]  (LSE * log2 e; +inf on padding rows)
   float* delta;    // workspace: fp32 [B*H, Npad]  (rowsum(dO * O); 0 on padding rows)
   const uint8_t* block_mask;  // device [nt][nt] (block-sparse backward) or nullptr
+  void* split_ws;             // split area of the workspace (BwdSplitWorkspace), or nullptr
+  size_t split_ws_bytes;
   DropoutParams drop;
   int* status;
   long long wait_limit;
@@ -125,14 +227,27 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Forward: plans the work (FwdGrid) and launches the variant it needs.
 cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream);
-// Variants compiled in their own translation units: the forward kernel with
-// dropout (a.drop.enabled != 0); the backward main kernel with a block mask,
-// with dropout, and with both.
-cudaError_t launch_fwd_dropout(const FwdLaunch& a, cudaStream_t stream);
-cudaError_t launch_bwd_main_sparse(const BwdLaunch& a, cudaStream_t stream);
-cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, cudaStream_t stream);
-cudaError_t launch_bwd_main_dropout_sparse(const BwdLaunch& a, cudaStream_t stream);
+// The forward variants, one translation unit each: plain without and with
+// dropout, sparse (block mask) and split (with the merge kernel after it).
+cudaError_t launch_fwd_plain(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_plain_dropout(const FwdLaunch& a, const FwdGrid& g, int grid,
+                                     cudaStream_t stream);
+cudaError_t launch_fwd_sparse(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_split(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream);
+// The backward main kernel's variants, one translation unit each: plain
+// (in fa_bwd.cu), sparse, plain with dropout, sparse with dropout, and split
+// (with or without dropout; with the merge kernel after it).
+cudaError_t launch_bwd_main_plain(const BwdLaunch& a, const BwdGrid& g, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_main_sparse(const BwdLaunch& a, const BwdGrid& g, int grid,
+                                   cudaStream_t stream);
+cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, const BwdGrid& g, int grid,
+                                    cudaStream_t stream);
+cudaError_t launch_bwd_main_dropout_sparse(const BwdLaunch& a, const BwdGrid& g, int grid,
+                                           cudaStream_t stream);
+cudaError_t launch_bwd_main_split(const BwdLaunch& a, const BwdGrid& g, int grid,
+                                  cudaStream_t stream);
 // Writes the keep decisions Z (1 = kept) of a.drop for [B*H, N, N] as bytes.
 cudaError_t launch_dropout_mask(const DropoutParams& drop, int BH, int N, uint8_t* keep,
                                 cudaStream_t stream);

@@ -51,6 +51,9 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                   0, stream);
   }
   if (need > static_cast<size_t>(FA_NOALLOC_SCRATCH_BYTES)) return FA_ERR_INVALID_ARG;
+  // Missing tensors are reported as fa_bwd reports them, before the scratch
+  // lookup touches the device.
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   void* scratch = scratch_on_current_device();
   if (scratch == nullptr) return FA_ERR_CUDA;
   // fa_bwd ignores the workspace's previous contents: its first stage

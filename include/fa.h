@@ -32,7 +32,11 @@
  *   - Errors: arguments are validated before anything is launched and
  *     nothing is written on error. FA_ERR_INVALID_ARG: a NULL pointer, B, H
  *     or N < 1, non-finite scale, a misaligned base address, an output that
- *     overlaps an input, or a workspace that is too small. FA_ERR_UNSUPPORTED:
+ *     shares an element with an input or with another output, or a workspace
+ *     that is too small. [B, H, N, d] tensors of one call are compared element
+ *     by element, so views that interleave in one buffer without sharing an
+ *     element (q, k, v or dq, dk, dv of a packed [B, N, 3, H, d] tensor) are
+ *     accepted; lse and workspaces by address range. FA_ERR_UNSUPPORTED:
  *     d not in {64, 128}, block_size != 128, or a device that is not sm_103.
  *     FA_ERR_CUDA: a CUDA call or launch failed. FA_ERR_DEVICE_TIMEOUT is
  *     reported by fa_device_status() when a bounded device-side wait expired.
@@ -72,11 +76,50 @@ int fa_fwd_kpad(const void* q, const void* k, const void* v, void* o, float* lse
                 int N, int d, int causal, float scale, const int32_t* kv_len,
                 struct CUstream_st* stream);
 
+/* Forward pass that may spread its last wave of work over every SM. The
+ * forward's work items are pairs of 128-row Q tiles; when their number is
+ * not a multiple of the SM count, the last round keeps only part of the GPU
+ * busy. Given a workspace, the items of that last round are cut into equal
+ * runs of K/V tiles, one run per SM (a stream-K schedule); each cut item's
+ * parts leave their unnormalised O and per-row running maximum and sum in
+ * the workspace, and a second kernel merges them with the same rescaling the
+ * online softmax applies from one K/V block to the next (condensed paper
+ * sample_paper.md section 3, "Softmax rescaling"). The pages themselves do
+ * not split the key range; this is a scheduling choice for small B*H or
+ * short sequences on a 152-SM GPU, and the result is the same attention.
+ *   fa_fwd_workspace_bytes: bytes of workspace with which fa_fwd_split (and
+ *     fa_attention_fwd_split) split these sizes on the current device; 0
+ *     when a split would not shorten the pass (then no workspace is needed).
+ *     Also 0 for invalid sizes.
+ *   fa_fwd_split: as fa_fwd_kpad, plus `workspace` (DEVICE, 16-byte aligned,
+ *     at least fa_fwd_workspace_bytes bytes, contents ignored; NULL with
+ *     workspace_bytes = 0 allowed). With a smaller or NULL workspace, with
+ *     kv_len != NULL, or when the split would not help, it runs exactly as
+ *     fa_fwd_kpad. The workspace must not overlap any tensor of the call.
+ *     Two calls that share a workspace must be ordered on the GPU. */
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal);
+int fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, const int32_t* kv_len, void* workspace,
+                 size_t workspace_bytes, struct CUstream_st* stream);
+
 /* Bytes of workspace fa_bwd needs: an fp32 dQ accumulator plus two fp32
  * per-row vectors (log2-scaled LSE and D = rowsum(dO * O)), each padded to a
  * multiple of 128 rows per head. Linear in N (sample_paper.md section 4:
  * memory linear in sequence length). Returns 0 for invalid sizes. */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/* Bytes of backward workspace with which the backward calls (fa_bwd,
+ * fa_bwd_main, fa_dropout_bwd, fa_attention_bwd) spread their last wave of
+ * work over every SM, as fa_fwd_split does for the forward: the key-tile
+ * items of the last round are cut into equal runs of Q tiles, each part
+ * adds its dQ into the accumulator as usual and leaves its dK, dV in the
+ * workspace, and a short kernel after the main kernel sums the parts. It is
+ * fa_bwd_workspace_bytes plus the parts' area when these sizes gain from the
+ * split on the current device, else fa_bwd_workspace_bytes. A workspace of
+ * at least this size enables the split; one of at least
+ * fa_bwd_workspace_bytes still works, without it. No split with kv_len or a
+ * block mask. 0 for invalid sizes. */
+size_t fa_bwd_split_workspace_bytes(int B, int H, int N, int d, int causal);
 
 /* Backward pass: gradients of L = sum(dO * O) with respect to Q, K, V. P is
  * recomputed on chip from Q, K and the forward's LSE instead of being read
@@ -88,7 +131,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  *   dq, dk, dv       : bf16 [B,H,N,d] outputs;
  *   kv_len           : DEVICE int32 [B] or NULL (as in fa_fwd_kpad);
  *   workspace        : DEVICE scratch of at least fa_bwd_workspace_bytes,
- *                      16-byte aligned; its contents on entry are ignored. */
+ *                      16-byte aligned; its contents on entry are ignored.
+ *                      With fa_bwd_split_workspace_bytes or more, the last
+ *                      wave of work is split over every SM (see there). */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
            const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
            float scale, const int32_t* kv_len, void* workspace, size_t workspace_bytes,
@@ -125,9 +170,10 @@ int fa_bwd_dq_convert(void* dq, int B, int H, int N, int d, void* workspace,
  * which every GPU that loads libfa.so holds until the process exits. The
  * caller still passes every input and output. Nothing is allocated or freed.
  *   - Limit: the call returns FA_ERR_INVALID_ARG, without launching, when
- *     fa_bwd_workspace_bytes(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES (for
- *     example B*H*Npad <= 254,200 rows at d = 64 and <= 129,055 at d = 128,
- *     Npad = N rounded up to a multiple of 128).
+ *     fa_bwd_workspace_bytes(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES, i.e.
+ *     when B*H*Npad (Npad = N rounded up to a multiple of 128) exceeds
+ *     254,080 rows at d = 64 or 129,024 rows at d = 128. NULL tensors are
+ *     rejected the same way, before the device is touched.
  *   - Set-up: the first call on each device, with that device current, looks
  *     up the buffer's device address (cudaGetSymbolAddress). Make that first
  *     call before any stream capture on that device.
@@ -245,6 +291,14 @@ typedef struct fa_attention_options {
 int fa_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                      int H, int N, int d, const fa_attention_options* opt,
                      struct CUstream_st* stream);
+
+/* fa_attention_fwd with a workspace for the split of the last wave, as
+ * fa_fwd_split (fa_fwd_workspace_bytes gives its size). No split with kv_len
+ * or a block mask; then, or with too small a workspace, exactly
+ * fa_attention_fwd. */
+int fa_attention_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, const fa_attention_options* opt,
+                           void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /* Backward pass of fa_attention_fwd with the same options (o and lse from
  * that call): dq, dk, dv in the same strides. Workspace and errors as fa_bwd. */

@@ -245,3 +245,74 @@ def test_sizes_beyond_32_bit_work_counts_rejected(L, B, H, N):
     assert L.fa_fwd(q, k, v, o, lse, B, H, N, 64, 0, 0.125, None) == 1
     assert L.fa_dropout_mask(B, H, N, 0.1, 1, 0, keep, None) == 1
 
+
+
+def test_split_workspace_queries(L):
+    import exact_io_aware_11_gb300 as fa
+    for d in (64, 128):
+        # one 128-row Q tile: nothing to split
+        assert fa.fwd_workspace_bytes(1, 1, 128, d, False) == 0
+        # two (b, h) problems of 4096 rows: 32 items for over a hundred SMs
+        assert fa.fwd_workspace_bytes(1, 2, 4096, d, True) > 0
+        base = fa.bwd_workspace_bytes(1, 2, 4096, d)
+        assert fa.bwd_split_workspace_bytes(1, 2, 4096, d, False) > base
+        assert fa.bwd_split_workspace_bytes(1, 1, 128, d, False) == fa.bwd_workspace_bytes(1, 1, 128, d)
+    for args in [(0, 1, 128, 64, 0), (1, 1, 128, 96, 0), (1, 1, 128, 64, 2), (1, 1, 0, 64, 0)]:
+        assert L.fa_fwd_workspace_bytes(*args) == 0
+        assert L.fa_bwd_split_workspace_bytes(*args) == 0
+
+
+def test_workspace_bytes_zero_for_unrepresentable_sizes(L):
+    # N near INT_MAX would overflow the tile rounding; B or H beyond 65535 is
+    # rejected by every entry point, so no workspace size exists for them.
+    assert L.fa_bwd_workspace_bytes(1, 1, (1 << 31) - 1, 64) == 0
+    assert L.fa_bwd_workspace_bytes(65536, 1, 128, 64) == 0
+    assert L.fa_bwd_workspace_bytes(1, 1, (1 << 31) - 256, 128) > 0
+
+
+@needs_cpu
+def test_noalloc_boundary_at_the_scratch_size(L):
+    # rows = B*H*Npad; d = 64 needs 4*64 + 8 bytes a row: 1985 heads of 128
+    # rows fit in 64 MiB, 1986 do not. The size check runs before any CUDA
+    # call, so without a GPU the call that fits reaches the device query
+    # (FA_ERR_CUDA) and the one that does not is rejected (FA_ERR_INVALID_ARG).
+    limit = 64 * 1024 * 1024
+    assert L.fa_bwd_workspace_bytes(1, 1985, 128, 64) <= limit
+    assert L.fa_bwd_workspace_bytes(1, 1986, 128, 64) > limit
+    assert L.fa_bwd_workspace_bytes(1, 1008, 128, 128) <= limit
+    assert L.fa_bwd_workspace_bytes(1, 1009, 128, 128) > limit
+    q, k, v, o, do, lse, dq, dk, dv = ptrs(9)
+    assert L.fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, 1, 1986, 128, 64, 0, 0.125, None,
+                            None) == 1
+    assert L.fa_bwd_noalloc(None, k, v, o, do, lse, dq, dk, dv, 1, 1985, 128, 64, 0, 0.125, None,
+                            None) == 1
+    assert L.fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, 1, 1985, 128, 64, 0, 0.125, None,
+                            None) == 3
+
+
+@needs_cpu
+def test_interleaved_views_accepted_overlapping_rejected(L):
+    """q, k, v (and dq, dk, dv) as the three slices of one packed [B, N, 3, H, d]
+    buffer share no element, so validation accepts them (and then fails only for
+    want of a device); outputs that do share elements are rejected."""
+    import ctypes
+    B, H, N, d = 2, 4, 256, 64
+    sb, sh, sn = N * 3 * H * d, d, 3 * H * d          # element strides of each slice
+    opt = _opts(stride_b=sb, stride_h=sh, stride_n=sn)
+    P, G, O, DO, LSE, WS = ptrs(6)                    # packed inputs, packed gradients, ...
+    q, k, v = P, P + 2 * H * d, P + 4 * H * d         # byte offsets of the slices
+    dq, dk, dv = G, G + 2 * H * d, G + 4 * H * d
+    o, do = O, O + 2 * H * d
+    need = L.fa_bwd_workspace_bytes(B, H, N, d)
+    rc = L.fa_attention_fwd(q, k, v, o, LSE, B, H, N, d, ctypes.byref(opt), None)
+    assert rc == 3
+    rc = L.fa_attention_bwd(q, k, v, o, do, LSE, dq, dk, dv, B, H, N, d, ctypes.byref(opt), WS,
+                            need, None)
+    assert rc == 3
+    # dk shifted by half a row onto dq's elements, or equal to dq: rejected
+    for bad_dk in (G + d, G):
+        rc = L.fa_attention_bwd(q, k, v, o, do, LSE, dq, bad_dk, dv, B, H, N, d,
+                                ctypes.byref(opt), WS, need, None)
+        assert rc == 1
+    # an output on an input's elements (o on k's slice): rejected
+    assert L.fa_attention_fwd(q, k, v, k, LSE, B, H, N, d, ctypes.byref(opt), None) == 1
