@@ -5,8 +5,12 @@
 
 One "step" is one pass of the hot path over one batch of the workload: the
 forward kernel, then the backward's preprocess, main and dQ-convert kernels.
-The headline workload is GPT-2-small-shaped causal attention (B=8, H=12,
-N=1024, d=64, bf16, seeded N(0,1) inputs). FLOPs per step follow the usual
+The headline workload is the largest single-GPU configuration: long-context
+non-causal attention with B=1, H=16, N=16384, d=128 (bf16 Q, K, V, dO drawn
+N(0, 0.5^2) from a seed, plus a per-head rank-8 bias on Q and K). The other
+configurations (GPT-2 small, BERT-large with key padding, N = 4K/8K
+causal and not, block-sparse at 16K, dropout, [B,N,H,d] storage, and the
+one-tile case) are timed in the sweep. FLOPs per step follow the usual
 count: forward 4*B*H*N^2*d, backward 2.5x that, both halved for causal.
 
 Timing: inputs resident in HBM; W untimed warm-up steps; then K steps, each
@@ -182,37 +186,53 @@ class Step:
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         self.dq, self.dk, self.dv = (like() for _ in range(3))
         self.opt = None
-        if w.layout != "bhnd":  # the general entry points take the strides
+        if w.layout != "bhnd" or w.dropout > 0:  # the general entry points take strides, dropout
             self.opt = fa.AttentionOptions()
             self.opt.stride_b, self.opt.stride_h, self.opt.stride_n = self.q.stride()[:3]
             self.opt.causal, self.opt.scale = int(w.causal), w.scale
-        self.ws_bytes = fa.bwd_workspace_bytes(B, H, N, d)
+            self.opt.dropout_p, self.opt.dropout_seed = w.dropout, w.dropout_seed
+            self.opt.block_size = 128
+        # backward workspace with room for the split of the last wave, and the
+        # forward's split workspace, where these sizes gain from the split
+        plain = self.kv is None and self.mask is None
+        base = fa.bwd_workspace_bytes(B, H, N, d)
+        self.ws_bytes = fa.bwd_split_workspace_bytes(B, H, N, d, w.causal) if plain else base
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.fws_bytes = fa.fwd_workspace_bytes(B, H, N, d, w.causal) if plain else 0
+        self.fws = (torch.empty(self.fws_bytes, dtype=torch.uint8, device=dev)
+                    if self.fws_bytes else None)
+        self.fwd_split = self.fws_bytes > 0
+        self.bwd_split = self.ws_bytes > base
         self.L = fa.lib()
         self.offset = 0  # dropout counter offset, advanced once per step
 
+    def launches(self):
+        """Kernels of one step: the forward (+ its merge when split), then the
+        backward's preprocess, main (+ merge when split) and dQ conversion."""
+        n = 1 + int(self.fwd_split)
+        if self.w.backward:
+            n += 3 + int(self.bwd_split)
+        return n
+
     def fwd(self, stream):
         w, L = self.w, self.L
+        fws = None if self.fws is None else self.fws.data_ptr()
         if self.opt is not None:
             import ctypes
-            rc = L.fa_attention_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
-                                    self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
-                                    ctypes.byref(self.opt), stream)
-        elif w.dropout > 0:
-            rc = L.fa_dropout_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
-                                  self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
-                                  int(w.causal), w.scale,
-                                  None if self.kv is None else self.kv.data_ptr(), w.dropout,
-                                  w.dropout_seed, self.offset, stream)
+            self.opt.dropout_offset = self.offset  # a fresh mask every step
+            rc = L.fa_attention_fwd_split(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                          self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N,
+                                          w.d, ctypes.byref(self.opt), fws, self.fws_bytes, stream)
         elif self.mask is not None:
             rc = L.fa_blocksparse_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
                                       self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
                                       w.scale, self.mask.data_ptr(), 128, stream)
         else:
-            rc = L.fa_fwd_kpad(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
-                               self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
-                               int(w.causal), w.scale,
-                               None if self.kv is None else self.kv.data_ptr(), stream)
+            rc = L.fa_fwd_split(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
+                                self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.N, w.d,
+                                int(w.causal), w.scale,
+                                None if self.kv is None else self.kv.data_ptr(), fws,
+                                self.fws_bytes, stream)
         assert rc == 0, rc
 
     def bwd_stages(self, stream):
@@ -224,18 +244,7 @@ class Step:
                                      self.dq.data_ptr(), self.dk.data_ptr(), self.dv.data_ptr(),
                                      w.B, w.H, w.N, w.d, ctypes.byref(self.opt),
                                      self.ws.data_ptr(), self.ws_bytes, stream)
-            yield 0
-            yield 0
-            return
-        if w.dropout > 0:  # one call runs all three kernels
-            yield L.fa_dropout_bwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(),
-                                   self.o.data_ptr(), self.do.data_ptr(), self.lse.data_ptr(),
-                                   self.dq.data_ptr(), self.dk.data_ptr(), self.dv.data_ptr(),
-                                   w.B, w.H, w.N, w.d, int(w.causal), w.scale,
-                                   None if self.kv is None else self.kv.data_ptr(), w.dropout,
-                                   w.dropout_seed, self.offset, self.ws.data_ptr(), self.ws_bytes,
-                                   stream)
-            self.offset += 1  # the next step draws a fresh mask
+            self.offset += 1
             yield 0
             yield 0
             return
@@ -332,7 +341,8 @@ def e2e_serial(fa, step: Step, steps: int, warmup: int):
         for n in names:
             dev_in[n].copy_(host_in[n], non_blocking=True)
         o, lse = fa.forward(dev_in["q"], dev_in["k"], dev_in["v"], causal=w.causal, scale=w.scale,
-                            kv_len=kv, out=outs[0], lse=outs[1])
+                            kv_len=kv, out=outs[0], lse=outs[1], workspace=step.fws,
+                            split=step.fwd_split)
         fa.backward(dev_in["q"], dev_in["k"], dev_in["v"], o, dev_in["dout"], lse,
                     causal=w.causal, scale=w.scale, kv_len=kv, workspace=step.ws, dq=outs[2],
                     dk=outs[3], dv=outs[4])
@@ -402,7 +412,7 @@ def e2e_pipelined(fa, step: Step, steps: int, warmup: int):
                 o, lse, dq, dk, dv = outs[s]
                 x = dev_in[s]
                 fa.forward(x["q"], x["k"], x["v"], causal=w.causal, scale=w.scale, kv_len=kv,
-                           out=o, lse=lse, stream=comp)
+                           out=o, lse=lse, stream=comp, workspace=step.fws, split=step.fwd_split)
                 fa.backward(x["q"], x["k"], x["v"], o, x["dout"], lse, causal=w.causal,
                             scale=w.scale, kv_len=kv, workspace=step.ws, dq=dq, dk=dk, dv=dv,
                             stream=comp)
@@ -439,6 +449,43 @@ def e2e_pipelined(fa, step: Step, steps: int, warmup: int):
     return ms, h2d, d2h
 
 
+def copy_rates(step: Step, reps: int = 5):
+    """Plain pinned-memory copy rates (GB/s) of the same tensors the
+    end-to-end leg moves each step: the inputs H2D alone, the outputs D2H
+    alone, and both at once on two streams (as the pipelined schedule
+    overlaps them), one cudaMemcpyAsync per tensor."""
+    dev = step.q.device
+    ins = [step.host[n] for n in ("q", "k", "v", "dout")]
+    h_in = [t.pin_memory() for t in ins]
+    d_in = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in ins]
+    d_out = [step.o, step.lse, step.dq, step.dk, step.dv]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in d_out]
+    nb_in = sum(t.numel() * t.element_size() for t in ins)
+    nb_out = sum(t.numel() * t.element_size() for t in d_out)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(do_up, do_down):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            if do_up:
+                with torch.cuda.stream(up):
+                    for d, h in zip(d_in, h_in):
+                        d.copy_(h, non_blocking=True)
+            if do_down:
+                with torch.cuda.stream(down):
+                    for h, d in zip(h_out, d_out):
+                        h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    run(True, True)  # warm-up
+    t_up, t_down, t_both = run(True, False), run(False, True), run(True, True)
+    return {"h2d_gbs": round(nb_in / t_up / 1e9, 1), "d2h_gbs": round(nb_out / t_down / 1e9, 1),
+            "both_ms": round(t_both * 1e3, 4),
+            "both_gbs": round((nb_in + nb_out) / t_both / 1e9, 1)}
+
+
 def e2e(fa, step: Step, steps: int, warmup: int):
     """End-to-end timing through the public API: the pipelined schedule, or the
     serial one if the pipelined run fails. Returns (ms per step, H2D bytes,
@@ -451,32 +498,57 @@ def e2e(fa, step: Step, steps: int, warmup: int):
 
 
 def cpu_baseline(w: W.Workload, budget_s: float = 12.0):
-    """Times the fp64 oracle (as it stands) on whole heads of the workload
-    until about `budget_s` seconds of CPU work; returns TFLOP/s."""
+    """Times the fp64 oracle (as it stands) on a bounded sample of the
+    workload, about `budget_s` seconds of CPU work; returns TFLOP/s.
+
+    Short sequences (N <= 2048): whole (b, h) heads, forward and backward.
+    Longer ones, where one head's backward alone would take minutes: the
+    forward of blocks of 256 query rows of a head of the workload (exact rows
+    of its attention), and the backward of the leading 2048 x 2048 problem of
+    that head, alternately."""
     import numpy as np
 
     import oracle
     x = W.make_inputs(w.with_(B=1, H=min(w.H, 4)), 0)
-    f_fwd, f_bwd = flops(w.with_(B=1, H=1))
-    done, t0, heads = 0.0, time.perf_counter(), 0
-    while True:
-        h = heads % x["q"].shape[1]
-        kv = None if x["kv_len"] is None else int(x["kv_len"][0])
-        oracle.head_forward(x["q"][0, h], x["k"][0, h], x["v"][0, h], w.scale, w.causal, kv)
-        done += f_fwd
-        if w.backward:
-            oracle.head_backward(x["q"][0, h], x["k"][0, h], x["v"][0, h], x["dout"][0, h],
-                                 w.scale, w.causal, kv)
-            done += f_bwd
-        heads += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
+    done, t0, heads, parts = 0.0, time.perf_counter(), 0, []
+    if w.N <= 2048:
+        f_fwd, f_bwd = flops(w.with_(B=1, H=1))
+        while True:
+            h = heads % x["q"].shape[1]
+            kv = None if x["kv_len"] is None else int(x["kv_len"][0])
+            oracle.head_forward(x["q"][0, h], x["k"][0, h], x["v"][0, h], w.scale, w.causal, kv)
+            done += f_fwd
+            if w.backward:
+                oracle.head_backward(x["q"][0, h], x["k"][0, h], x["v"][0, h], x["dout"][0, h],
+                                     w.scale, w.causal, kv)
+                done += f_bwd
+            heads += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+        sample = (f"{heads} whole (b,h) heads of {w.name} (N={w.N}, d={w.d}, "
+                  f"{'fwd+bwd' if w.backward else 'fwd'}), numpy fp64, {el:.1f} s")
+    else:
+        q, k, v, do = (x[n][0, 0] for n in ("q", "k", "v", "dout"))
+        ns, r0, nrows, nbwd = 2048, 0, 0, 0
+        while True:
+            rows = np.arange(r0, r0 + 256) % w.N
+            oracle.head_forward(q, k, v, w.scale, w.causal, rows=rows)
+            seen = (rows + 1) if w.causal else np.full(len(rows), w.N)
+            done += float(4.0 * w.d * seen.sum())
+            r0 += 256
+            nrows += 256
+            if w.backward:
+                oracle.head_backward(q[:ns], k[:ns], v[:ns], do[:ns], w.scale, w.causal)
+                done += 2.5 * 4.0 * ns * ns * w.d / (2 if w.causal else 1)
+                nbwd += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+        sample = (f"{w.name}: forward of {nrows} query rows of one head (N={w.N}, d={w.d}) and "
+                  f"{nbwd} backward passes of its leading {ns}x{ns} problem, numpy fp64, {el:.1f} s")
     return {"value": done / el / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{heads} whole (b,h) heads of {w.name} (N={w.N}, d={w.d}, "
-                      f"{'fwd+bwd' if w.backward else 'fwd'}), numpy fp64, {el:.1f} s",
-            "seconds": el}
+            "kind": "oracle", "sample": sample, "seconds": el}
 
 
 def dist_setup(args):
@@ -552,16 +624,22 @@ def run_ours(args, world, rank, local):
     dom = max(per_kernel, key=per_kernel.get)
     dom_flops = {"fwd": f_fwd, "bwd_main": f_bwd}.get(dom)
     peak_tf = pk["bf16_tflops"]
+    # The kernel is timed inside a long run of steps, so its roofline takes the
+    # sustained bf16 figure; the fraction of the burst figure is given beside it.
+    peak_sus = pk.get("bf16_tflops_sustained", peak_tf)
     roofline = None
     if dom_flops is not None:
         ach = dom_flops / (per_kernel[dom] * 1e-3) / 1e12
         roofline = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2),
-                    "peak": peak_tf, "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4),
-                    "peak_kind": f"{pk_kind} bf16 dense (burst)",
+                    "peak": peak_sus, "unit": "TFLOP/s", "frac": round(ach / peak_sus, 4),
+                    "peak_kind": f"{pk_kind} bf16 dense, sustained (kernel timed inside a long run "
+                                 f"of steps)",
+                    "frac_of_burst": round(ach / peak_tf, 4),
                     "traffic": ncu_traffic(dom, w.name)}
 
     e2e_ms, h2d, d2h, e2e_sched = (e2e(fa, step, max(3, args.steps // 4), 3) if w.backward
                                    else (None, 0, 0, None))
+    copies = copy_rates(step) if w.backward else None
     clk = clocks.stop(window=tuple(t_region))
 
     out = {
@@ -573,7 +651,8 @@ def run_ours(args, world, rank, local):
         "config": {"workload": f"{w.name}: {'causal' if w.causal else 'non-causal'} fwd+bwd, "
                                f"B={w.B} H={w.H} N={w.N} d={w.d}",
                    "pass": "fwd + bwd (preprocess, main, dQ convert)",
-                   "launch": "programmatic dependent launch between the four kernels",
+                   "launch": "programmatic dependent launch between the kernels",
+                   "split": {"fwd": step.fwd_split, "bwd": step.bwd_split},
                    "l2": "flushed between timed steps (256 MiB write)",
                    "parallelism": f"replicas x{world} (independent (b,h) problems, no collective)"},
         "pct_of_bf16_peak": round(value / world / peak_tf, 4),
@@ -581,7 +660,7 @@ def run_ours(args, world, rank, local):
         "per_kernel_timing": "second pass of the same steps with an event between kernels "
                              "(no launch overlap); ms_per_step is the whole-step timing",
         "fwd_tflops": round(f_fwd / (per_kernel["fwd"] * 1e-3) / 1e12, 2),
-        "gpu_launches": args.steps * len(per_kernel),
+        "gpu_launches": args.steps * step.launches(),
         "roofline": roofline,
         "clocks": clk,
     }
@@ -589,28 +668,35 @@ def run_ours(args, world, rank, local):
         e2e_value, e2e_ms = whole_job_tflops(world, step_flops, e2e_ms)
         out["e2e"] = {"value": round(e2e_value, 3),
                       "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                      "ms_per_step": round(e2e_ms, 4), "schedule": e2e_sched}
+                      "ms_per_step": round(e2e_ms, 4), "schedule": e2e_sched,
+                      "copy_gbs": round((h2d + d2h) / (e2e_ms * 1e-3) / 1e9, 1),
+                      "plain_copy": copies}
     if args.sweep and rank == 0:
-        out["sweep"] = sweep(fa, dev, flush, pk)
+        out["sweep"] = sweep(fa, dev, flush, pk, w.name)
     if rank == 0 and world == 1:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
     return out
 
 
-def sweep(fa, dev, flush, pk):
-    """Fwd and bwd TFLOP/s of every workload (few steps each)."""
+def sweep(fa, dev, flush, pk, headline):
+    """Fwd and bwd TFLOP/s of every other workload (few steps each)."""
     res = {}
     for name, w in W.WORKLOADS.items():
-        if name == "gpt2_small":
+        if name == headline:
             continue
         st = Step(fa, w, 0, dev)
         t = time_steps(st, 10, 3, flush, backward=w.backward)
+        whole = time_steps(st, 10, 3, flush, backward=w.backward, split=False)["step"]
         f_fwd, f_bwd = flops(w)
         if w.sparse:  # effective work: kept blocks only
             f_fwd = 4.0 * w.B * w.H * w.d * 128 * 128 * int(st.host["block_mask"].sum())
             f_bwd = 2.5 * f_fwd
         r = {"fwd_ms": round(statistics.median(t["fwd"]), 4),
-             "fwd_tflops": round(f_fwd / (statistics.median(t["fwd"]) * 1e-3) / 1e12, 2)}
+             "fwd_tflops": round(f_fwd / (statistics.median(t["fwd"]) * 1e-3) / 1e12, 2),
+             "split": {"fwd": st.fwd_split, "bwd": st.bwd_split}}
+        step_ms = statistics.median(whole)
+        r["step_ms"] = round(step_ms, 4)  # whole step, kernels chained by dependent launch
+        r["step_tflops"] = round((f_fwd + (f_bwd if w.backward else 0.0)) / (step_ms * 1e-3) / 1e12, 2)
         r["fwd_pct_peak"] = round(r["fwd_tflops"] / pk["bf16_tflops"], 4)
         eff = None
         if st.host["kv_len"] is not None and not w.causal:  # the kernels skip padded key tiles
@@ -626,9 +712,7 @@ def sweep(fa, dev, flush, pk):
                 r["bwd_tflops_effective"] = round(eff[1] / (mb * 1e-3) / 1e12, 2)
             if w.sparse:
                 r["bwd_timing"] = "one fa_blocksparse_bwd call (preprocess, main, dQ convert)"
-            elif w.dropout > 0:
-                r["bwd_timing"] = "one fa_dropout_bwd call (preprocess, main, dQ convert)"
-            elif w.layout != "bhnd":
+            elif w.dropout > 0 or w.layout != "bhnd":
                 r["bwd_timing"] = "one fa_attention_bwd call (preprocess, main, dQ convert)"
             else:
                 r["bwd_main_ms"] = round(statistics.median(t["bwd_main"]), 4)
@@ -673,7 +757,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gpt2_small", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="long_n16384_noncausal", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--soak", type=float, default=1.0,

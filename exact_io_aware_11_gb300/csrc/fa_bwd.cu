@@ -63,10 +63,18 @@ cudaError_t launch_main(const BwdLaunch& a, cudaStream_t stream) {
                        a.block_mask == nullptr;
   g.plan = plan_bwd(a.B, a.H, a.N, a.d, a.causal != 0, sms, allowed);
   if (g.plan.whole < g.plan.n_items) {
-    uint8_t* w = static_cast<uint8_t*>(a.split_ws);
-    g.slot_item = reinterpret_cast<int*>(w + ws.slot_off);
-    g.dkv_part = reinterpret_cast<float*>(w + ws.dkv_off);
-    return launch_bwd_main_split(a, g, sms, stream);
+    // Whole rounds on the plain kernel, then the tail on the split kernel.
+    g.dkv_part = reinterpret_cast<float*>(static_cast<uint8_t*>(a.split_ws) + ws.dkv_off);
+    if (g.plan.whole > 0) {
+      const cudaError_t e = a.drop.enabled ? launch_bwd_main_dropout(a, g, sms, stream)
+                                           : launch_bwd_main_plain(a, g, sms, stream);
+      if (e != cudaSuccess) return e;
+    }
+    const int nt = g.nt, BH = g.BH;
+    const bool causal = a.causal != 0;
+    const MergeTable m =
+        build_merge_table(g.plan, [&](int k) { return bwd_item_steps(nt, BH, causal, k); });
+    return launch_bwd_main_split(a, g, g.plan.tail_ctas, m, stream);
   }
   const int grid = min(g.n_items, sms);
   if (a.block_mask != nullptr)

@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto steps = [&](int k) { return bwd_steps<CAUSAL>(grid, k); };
   if constexpr (MODE == kModeSplit) {
     if (warp == 8) {
-      const TailRange tr = tail_range(grid.plan, blockIdx.x, gridDim.x, steps);
+      const TailRange tr = tail_range(grid.plan, blockIdx.x, steps);
       if (lane == 0) *tail_sh = tr;
     }
   }
@@ -366,24 +366,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
   grid_dep_launch();
   const Watchdog wd{wait_limit, status, abort_flag};
-  if constexpr (MODE == kModeSplit) {
-    if (threadIdx.x == 0) {
-      const TailRange tr = *tail_sh;
-      write_slot_items(grid.slot_item, tr, blockIdx.x, tr.t1 >= tr.t0 ? steps(tr.t0) : 0,
-                       tr.t1 >= tr.t0 ? steps(tr.t1) : 0);
-    }
-  }
-  // The r-th unit of this CTA, or a unit with k < 0: whole items in a snake
-  // over the item list, and for a split plan the parts of its tail.
+  // The r-th unit of this CTA, or a unit with k < 0: the split kernel runs
+  // the CTA's run of the tail; the others whole items [0, plan.whole) in a
+  // snake over the item list.
   auto unit = [&](int r) -> Unit {
     if constexpr (MODE == kModeSplit) {
-      return unit_of(grid.plan, tail_sh, r, blockIdx.x, gridDim.x, steps);
+      return tail_unit(tail_sh, r, blockIdx.x, steps);
     } else {
       Unit u{-1, 0, 1 << 30, -1};
       const int G = gridDim.x, c = blockIdx.x;
-      if (r * G >= grid.n_items) return u;
+      if (r * G >= grid.plan.whole) return u;
       const int k = r * G + ((r & 1) ? G - 1 - c : c);
-      if (k < grid.n_items) u.k = k;
+      if (k < grid.plan.whole) u.k = k;
       return u;
     }
   };
@@ -868,33 +862,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Sums the parts of the split backward items: block s handles the key tile
-// in workspace slot s if s is the first slot holding part of it, one thread
-// per (dK or dV, key row), and writes dK = sum of the parts' dK (already
-// scaled) and dV = sum of their dV, bf16. Every part covers a different run
-// of Q tiles, so the sums are the whole accumulations
+// Sums the parts of the backward items cut by a split plan: block (i, c)
+// handles columns [32 c, 32 c + 32) of cut key tile i of the merge table, one
+// thread per (dV or dK, key row), and writes dK = sum of the parts' dK
+// (already scaled) and dV = sum of their dV, bf16. Every part covers a
+// different run of Q tiles, so the sums are the whole accumulations
 // dK_j = scale sum_i dS_ij^T Q_i and dV_j = sum_i P_ij^T dO_i.
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256) bwd_merge_kernel(BwdGrid g, __nv_bfloat16* __restrict__ dk,
-                                                        __nv_bfloat16* __restrict__ dv, int n_slots) {
-  grid_dep_wait();  // the main kernel's parts are complete
+__global__ void __launch_bounds__(256) bwd_merge_kernel(BwdGrid g, const __grid_constant__ MergeTable m,
+                                                        __nv_bfloat16* __restrict__ dk,
+                                                        __nv_bfloat16* __restrict__ dv) {
+  grid_dep_wait();  // the split kernel's parts are complete
   grid_dep_launch();
-  const int s = blockIdx.x;
-  int s_last = s;
-  if (merge_slots(g.slot_item, n_slots, s, s_last) == 0) return;
-  const int t = g.slot_item[s];
+  const int i = blockIdx.x, c0 = blockIdx.y * 32;
+  const int t = m.item[i], q0 = m.first[i], q1 = m.first[i + 1];
   int bh, j;
   bwd_item_coords(g.nt, g.BH, CAUSAL, t, bh, j);
   const int which = threadIdx.x >> 7, rr = threadIdx.x & 127;  // which: 0 dV, 1 dK
-  float acc[D];
+  float acc[32];
 #pragma unroll
-  for (int c = 0; c < D; ++c) acc[c] = 0.f;
-  for (int q = s; q <= s_last; ++q) {
-    if (g.slot_item[q] != t) continue;
+  for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+  for (int q = q0; q < q1; ++q) {
     const float4* src = reinterpret_cast<const float4*>(g.dkv_part) +
-                        (static_cast<size_t>(q) * 2 + which) * (D / 4) * kBlock + rr;
+                        ((static_cast<size_t>(m.slot[q]) * 2 + which) * (D / 4) + c0 / 4) * kBlock + rr;
 #pragma unroll
-    for (int c = 0; c < D / 4; ++c) {
+    for (int c = 0; c < 8; ++c) {
       const float4 a = src[c * kBlock];
       acc[4 * c] += a.x;
       acc[4 * c + 1] += a.y;
@@ -904,15 +896,14 @@ __global__ void __launch_bounds__(256) bwd_merge_kernel(BwdGrid g, __nv_bfloat16
   }
   const int key = j * kBlock + rr;
   if (key >= g.N) return;
-  uint4* dst = reinterpret_cast<uint4*>((which ? dk : dv) + row_offset(g.st, g.H, bh, key));
+  uint4* dst = reinterpret_cast<uint4*>((which ? dk : dv) + row_offset(g.st, g.H, bh, key) + c0);
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c)
+  for (int c = 0; c < 4; ++c)
     dst[c] = make_uint4(pack_bf16(acc[8 * c], acc[8 * c + 1]), pack_bf16(acc[8 * c + 2], acc[8 * c + 3]),
                         pack_bf16(acc[8 * c + 4], acc[8 * c + 5]), pack_bf16(acc[8 * c + 6], acc[8 * c + 7]));
 }
 
-// Launches bwd_main_kernel<D, CAUSAL, MODE, DROP> on `grid` CTAs (and, for
-// the split variant, the merge kernel after it).
+// Launches bwd_main_kernel<D, CAUSAL, MODE, DROP> on `grid` CTAs.
 template <int D, bool CAUSAL, int MODE, bool DROP>
 cudaError_t launch_bwd_main_kernel(const BwdLaunch& a, const BwdGrid& g, int grid,
                                    cudaStream_t stream) {
@@ -921,12 +912,20 @@ cudaError_t launch_bwd_main_kernel(const BwdLaunch& a, const BwdGrid& g, int gri
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = set_smem_once(smem_set, reinterpret_cast<const void*>(kern), L::kSmem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kern, dim3(grid), dim3(kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
-                 a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g, g.nt * kBlock, a.scale,
-                 a.drop, a.status, a.wait_limit);
-  if (e != cudaSuccess || MODE != kModeSplit) return e;
-  return launch_pdl(bwd_merge_kernel<D, CAUSAL>, dim3(2 * grid), dim3(256), 0, stream, g,
-                    static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv), 2 * grid);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
+                    a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g, g.nt * kBlock, a.scale,
+                    a.drop, a.status, a.wait_limit);
+}
+
+// The split kernel over the tail on `grid` (= plan.tail_ctas) CTAs, then the
+// merge kernel over the cut items of `m`.
+template <int D, bool CAUSAL, bool DROP>
+cudaError_t launch_bwd_tail(const BwdLaunch& a, const BwdGrid& g, int grid, const MergeTable& m,
+                            cudaStream_t stream) {
+  cudaError_t e = launch_bwd_main_kernel<D, CAUSAL, kModeSplit, DROP>(a, g, grid, stream);
+  if (e != cudaSuccess || m.n == 0) return e;
+  return launch_pdl(bwd_merge_kernel<D, CAUSAL>, dim3(m.n, D / 32), dim3(256), 0, stream, g, m,
+                    static_cast<__nv_bfloat16*>(a.dk), static_cast<__nv_bfloat16*>(a.dv));
 }
 
 // The (d, causal) variants of one mode and dropout setting.

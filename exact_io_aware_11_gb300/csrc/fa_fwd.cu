@@ -23,12 +23,21 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
                        a.block_mask == nullptr;
   g.plan = plan_fwd(a.B, a.H, a.N, a.d, a.causal != 0, sms, allowed);
   if (g.plan.whole < g.plan.n_items) {
+    // Whole rounds on the plain kernel, then the tail on the split kernel.
     uint8_t* w = static_cast<uint8_t*>(a.split_ws);
-    g.slot_item = reinterpret_cast<int*>(w + ws.slot_off);
     g.m_part = reinterpret_cast<float*>(w + ws.m_off);
     g.l_part = reinterpret_cast<float*>(w + ws.l_off);
     g.o_part = reinterpret_cast<float*>(w + ws.o_off);
-    return launch_fwd_split(a, g, sms, stream);
+    if (g.plan.whole > 0) {
+      const cudaError_t e = a.drop.enabled ? launch_fwd_plain_dropout(a, g, sms, stream)
+                                           : launch_fwd_plain(a, g, sms, stream);
+      if (e != cudaSuccess) return e;
+    }
+    const int nqt = g.nqt, npairs = g.npairs, BH = g.n_items / g.npairs;
+    const bool causal = a.causal != 0;
+    const MergeTable m = build_merge_table(
+        g.plan, [&](int k) { return fwd_item_steps(nqt, npairs, BH, causal, k); });
+    return launch_fwd_split(a, g, g.plan.tail_ctas, m, stream);
   }
   const int grid = min(g.n_items, sms);
   if (a.block_mask != nullptr) return launch_fwd_sparse(a, g, grid, stream);

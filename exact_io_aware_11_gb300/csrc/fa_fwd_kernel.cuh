@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   auto steps = [&](int k) { return fwd_steps<CAUSAL>(g, k); };
   if constexpr (MODE == kModeSplit) {
     if (warp == kLoadWarp) {
-      const TailRange tr = tail_range(g.plan, blockIdx.x, gridDim.x, steps);
+      const TailRange tr = tail_range(g.plan, blockIdx.x, steps);
       if (lane == 0) *tail_sh = tr;
     }
   }
@@ -248,24 +248,18 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
   grid_dep_launch();
   const Watchdog wd{wait_limit, status, abort_flag};
-  if constexpr (MODE == kModeSplit) {
-    if (threadIdx.x == 0) {
-      const TailRange tr = *tail_sh;
-      write_slot_items(g.slot_item, tr, blockIdx.x, tr.t1 >= tr.t0 ? steps(tr.t0) : 0,
-                       tr.t1 >= tr.t0 ? steps(tr.t1) : 0);
-    }
-  }
-  // The r-th unit of this CTA, or a unit with k < 0: whole items in a snake
-  // over the item list, and for a split plan the parts of its tail.
+  // The r-th unit of this CTA, or a unit with k < 0: the split kernel runs
+  // the CTA's run of the tail; the others whole items [0, plan.whole) in a
+  // snake over the item list.
   auto unit = [&](int r) -> Unit {
     if constexpr (MODE == kModeSplit) {
-      return unit_of(g.plan, tail_sh, r, blockIdx.x, gridDim.x, steps);
+      return tail_unit(tail_sh, r, blockIdx.x, steps);
     } else {
       Unit u{-1, 0, 1 << 30, -1};
       const int G = gridDim.x, c = blockIdx.x;
-      if (r * G >= g.n_items) return u;
+      if (r * G >= g.plan.whole) return u;
       const int k = r * G + ((r & 1) ? G - 1 - c : c);
-      if (k < g.n_items) u.k = k;  // only the last round can run past the end
+      if (k < g.plan.whole) u.k = k;  // only the last round can run past the end
       return u;
     }
   };
@@ -880,68 +874,70 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   }
 }
 
-// Merges the parts of the split items. Block s handles the item in
-// workspace slot s if s is the first slot that holds part of it, one thread
-// per row of its two Q tiles: with m_q, l_q, O_q the running maximum (log2
+// Merges the parts of the items cut by a split plan. Block (i, c) handles
+// columns [32 c, 32 c + 32) of cut item i of the merge table, one thread per
+// row of its two Q tiles: with m_q, l_q, O_q the running maximum (log2
 // units), sum and unnormalised output of part q of the row, M = max_q m_q and
 //   O = r sum_q 2^(m_q - M) O_q / sum_q 2^(m_q - M) l_q,
 //   LSE = (M + log2 sum_q 2^(m_q - M) l_q) ln 2,
 // which is the online-softmax rescaling applied once more, across the parts
 // (r = 1 / (1 - p') with dropout, else 1). Parts that saw no key (l = 0) do
 // not contribute; a row with no part left gets O = 0 and LSE = -inf. The
-// partial O is read column-group major, 512 contiguous bytes per warp load.
+// partial O is read column-group major (512 contiguous bytes per warp load)
+// and each thread writes 64 contiguous bytes of its output row.
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(256) fwd_merge_kernel(FwdGrid g, __nv_bfloat16* __restrict__ out,
-                                                        float* __restrict__ lse_out, int n_slots,
-                                                        float rescale) {
-  grid_dep_wait();  // the main kernel's parts are complete
+__global__ void __launch_bounds__(256) fwd_merge_kernel(FwdGrid g, const __grid_constant__ MergeTable m,
+                                                        __nv_bfloat16* __restrict__ out,
+                                                        float* __restrict__ lse_out, float rescale) {
+  grid_dep_wait();  // the split kernel's parts are complete
   grid_dep_launch();
-  const int s = blockIdx.x;
-  int s_last = s;
-  if (merge_slots(g.slot_item, n_slots, s, s_last) == 0) return;
-  const int t = g.slot_item[s];
+  const int i = blockIdx.x, c0 = blockIdx.y * 32;
+  const int t = m.item[i], q0 = m.first[i], q1 = m.first[i + 1];
   int bh, p;
   fwd_item_coords(g.npairs, g.n_items / g.npairs, CAUSAL, t, bh, p);
   const int x = threadIdx.x;  // row of the pair: tile x / 128, row x % 128
   const int qt = 2 * p + (x >> 7), row = qt * kBlock + (x & 127);
   float M = -INFINITY;
-  for (int q = s; q <= s_last; ++q)
-    if (g.slot_item[q] == t && g.l_part[static_cast<size_t>(q) * 256 + x] > 0.f)
-      M = fmaxf(M, g.m_part[static_cast<size_t>(q) * 256 + x]);
+  for (int q = q0; q < q1; ++q) {
+    const size_t pr = static_cast<size_t>(m.slot[q]) * 256 + x;
+    if (g.l_part[pr] > 0.f) M = fmaxf(M, g.m_part[pr]);
+  }
   float Lsum = 0.f;
-  float acc[D];
+  float acc[32];
 #pragma unroll
-  for (int c = 0; c < D; ++c) acc[c] = 0.f;
-  for (int q = s; q <= s_last; ++q) {
-    if (g.slot_item[q] != t) continue;
-    const float l = g.l_part[static_cast<size_t>(q) * 256 + x];
-    if (!(l > 0.f)) continue;
-    const float w = exp2f(g.m_part[static_cast<size_t>(q) * 256 + x] - M);
+  for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+  for (int q = q0; q < q1; ++q) {
+    const int sl = m.slot[q];
+    const float l = g.l_part[static_cast<size_t>(sl) * 256 + x];
+    const float w = l > 0.f ? exp2f(g.m_part[static_cast<size_t>(sl) * 256 + x] - M) : 0.f;
     Lsum += w * l;
-    const float4* src = reinterpret_cast<const float4*>(g.o_part) + static_cast<size_t>(q) * (D / 4) * 256 + x;
+    const float4* src = reinterpret_cast<const float4*>(g.o_part) +
+                        (static_cast<size_t>(sl) * (D / 4) + c0 / 4) * 256 + x;
+    if (w > 0.f) {
 #pragma unroll
-    for (int c = 0; c < D / 4; ++c) {
-      const float4 a = src[c * 256];
-      acc[4 * c] += w * a.x;
-      acc[4 * c + 1] += w * a.y;
-      acc[4 * c + 2] += w * a.z;
-      acc[4 * c + 3] += w * a.w;
+      for (int c = 0; c < 8; ++c) {
+        const float4 a = src[c * 256];
+        acc[4 * c] += w * a.x;
+        acc[4 * c + 1] += w * a.y;
+        acc[4 * c + 2] += w * a.z;
+        acc[4 * c + 3] += w * a.w;
+      }
     }
   }
   if (qt >= g.nqt || row >= g.N) return;
-  lse_out[static_cast<size_t>(bh) * g.N + row] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+  if (c0 == 0)
+    lse_out[static_cast<size_t>(bh) * g.N + row] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
   const float inv = Lsum > 0.f ? rescale / Lsum : 0.f;
-  uint4* dst = reinterpret_cast<uint4*>(out + row_offset(g.st, g.H, bh, row));
+  uint4* dst = reinterpret_cast<uint4*>(out + row_offset(g.st, g.H, bh, row) + c0);
 #pragma unroll
-  for (int c = 0; c < D / 8; ++c)
+  for (int c = 0; c < 4; ++c)
     dst[c] = make_uint4(pack_bf16(acc[8 * c] * inv, acc[8 * c + 1] * inv),
                         pack_bf16(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
                         pack_bf16(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv),
                         pack_bf16(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
 }
 
-// Launches fwd_kernel<D, CAUSAL, DROP, MODE> on `grid` CTAs (and, for the
-// split variant, the merge kernel after it).
+// Launches fwd_kernel<D, CAUSAL, DROP, MODE> on `grid` CTAs.
 template <int D, bool CAUSAL, bool DROP, int MODE>
 cudaError_t launch_fwd_kernel(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream) {
   using L = FwdLayout<D>;
@@ -950,12 +946,19 @@ cudaError_t launch_fwd_kernel(const FwdLaunch& a, const FwdGrid& g, int grid, cu
   cudaError_t e = set_smem_once(smem_set, reinterpret_cast<const void*>(kern), L::kSmem);
   if (e != cudaSuccess) return e;
   const float scale_log2 = a.scale * 1.4426950408889634f;
-  e = launch_pdl(kern, dim3(grid), dim3(FwdWarps<D>::kThreads), L::kSmem, stream, a.tm_q, a.tm_k,
-                 a.tm_v, a.o, a.lse, g, scale_log2, a.drop, a.status, a.wait_limit);
-  if (e != cudaSuccess || MODE != kModeSplit) return e;
-  return launch_pdl(fwd_merge_kernel<D, CAUSAL>, dim3(2 * grid), dim3(256), 0, stream, g,
-                    static_cast<__nv_bfloat16*>(a.o), a.lse, 2 * grid,
-                    a.drop.enabled ? a.drop.rescale : 1.f);
+  return launch_pdl(kern, dim3(grid), dim3(FwdWarps<D>::kThreads), L::kSmem, stream, a.tm_q, a.tm_k,
+                    a.tm_v, a.o, a.lse, g, scale_log2, a.drop, a.status, a.wait_limit);
+}
+
+// The split kernel over the tail on `grid` (= plan.tail_ctas) CTAs, then the
+// merge kernel over the cut items of `m`.
+template <int D, bool CAUSAL, bool DROP>
+cudaError_t launch_fwd_tail(const FwdLaunch& a, const FwdGrid& g, int grid, const MergeTable& m,
+                            cudaStream_t stream) {
+  cudaError_t e = launch_fwd_kernel<D, CAUSAL, DROP, kModeSplit>(a, g, grid, stream);
+  if (e != cudaSuccess || m.n == 0) return e;
+  return launch_pdl(fwd_merge_kernel<D, CAUSAL>, dim3(m.n, D / 32), dim3(256), 0, stream, g, m,
+                    static_cast<__nv_bfloat16*>(a.o), a.lse, a.drop.enabled ? a.drop.rescale : 1.f);
 }
 
 // The (d, causal) variants of one dropout setting and mode.

@@ -46,12 +46,13 @@ __host__ __device__ __forceinline__ long long row_offset(const Strides& s, int H
 }
 
 // How a persistent kernel's work items are shared out over its G CTAs
-// (fa_sched.cuh). Items [0, whole) are handed out whole, round r to CTA
-// (r odd ? G-1-c : c) of item r G + c (a snake over an item list ordered
-// heaviest first, so that CTAs get similar totals). When whole < n_items the
-// items [whole, n_items) form the tail: they are laid end to end as steps and
-// CTAs 0 .. tail_ctas - 1 take equal runs of them; whole is then a multiple
-// of G. When whole == n_items nothing is split and the last round may be short.
+// (fa_sched.cuh). Items [0, whole) are handed out whole by the plain kernel,
+// round r to CTA (r odd ? G-1-c : c) of item r G + c (a snake over an item
+// list ordered heaviest first, so that CTAs get similar totals). When
+// whole < n_items, the items [whole, n_items) form the tail: a second launch
+// of the split kernel, with tail_ctas CTAs, lays them end to end as steps and
+// gives each CTA an equal run; whole is then a multiple of G. When
+// whole == n_items nothing is split and the last round may be short.
 struct SplitPlan {
   int n_items;
   int whole;
@@ -63,6 +64,17 @@ struct SplitPlan {
 // including) step o1 of item t1; no tail work when t1 < t0.
 struct TailRange {
   int t0, o0, t1, o1;
+};
+
+// Which workspace slots hold the parts of each item cut by a split plan, for
+// the merge kernels (block i merges item[i] from the slots
+// slot[first[i] .. first[i + 1])). Built on the host (fa_sched.cuh).
+constexpr int kMaxSplitCtas = 256;
+struct MergeTable {
+  int n;
+  int item[kMaxSplitCtas];
+  short first[kMaxSplitCtas + 1];
+  short slot[2 * kMaxSplitCtas];
 };
 
 // Compile-time variants of the persistent kernels: plain (whole items, dense
@@ -82,19 +94,18 @@ struct DropoutParams {
   int enabled;        // 0: no dropout (the other fields are ignored)
 };
 
-// Workspace of a split forward (see fa_sched.cuh): per CTA two slots, each
-// holding one partial result of a pair of Q tiles -- the tail item it belongs
-// to, and per row the running maximum, the running sum and the unnormalised
-// O (fp32). Regions are 256-byte aligned.
+// Workspace of a split forward (see fa_sched.cuh): per CTA of the split
+// kernel two slots, each holding one partial result of a pair of Q tiles --
+// per row the running maximum, the running sum and the unnormalised O
+// (fp32). Regions are 256-byte aligned.
 struct FwdSplitWorkspace {
-  size_t slot_off, m_off, l_off, o_off, total;
+  size_t m_off, l_off, o_off, total;
 };
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 inline FwdSplitWorkspace fwd_split_layout(int G, int d) {
   FwdSplitWorkspace w{};
   const size_t slots = 2 * static_cast<size_t>(G);
-  w.slot_off = 0;
-  w.m_off = align256(slots * 4);
+  w.m_off = 0;
   w.l_off = w.m_off + align256(slots * 256 * 4);
   w.o_off = w.l_off + align256(slots * 256 * 4);
   w.total = w.o_off + align256(slots * 256 * static_cast<size_t>(d) * 4);
@@ -102,16 +113,15 @@ inline FwdSplitWorkspace fwd_split_layout(int G, int d) {
 }
 
 // Extra workspace of a split backward, placed after the regions of
-// BwdWorkspace: per slot the tail item it holds and a partial dK, dV (fp32,
-// 128 key rows x d each, dK already multiplied by the scale).
+// BwdWorkspace: per slot a partial dV, dK (fp32, 128 key rows x d each, dK
+// already multiplied by the scale).
 struct BwdSplitWorkspace {
-  size_t slot_off, dkv_off, total;  // offsets from the start of the split area
+  size_t dkv_off, total;  // offsets from the start of the split area
 };
 inline BwdSplitWorkspace bwd_split_layout(int G, int d) {
   BwdSplitWorkspace w{};
   const size_t slots = 2 * static_cast<size_t>(G);
-  w.slot_off = 0;
-  w.dkv_off = align256(slots * 4);
+  w.dkv_off = 0;
   w.total = w.dkv_off + align256(slots * 2 * 128 * static_cast<size_t>(d) * 4);
   return w;
 }
@@ -137,7 +147,6 @@ struct FwdGrid {
   const uint8_t* block_mask;
   SplitPlan plan;
   // split plans only: workspace slots of the partial results
-  int* slot_item;  // [2G] tail item held by each slot, or -1
   float* m_part;   // [2G][256] running maximum (log2 units) of each row
   float* l_part;   // [2G][256] running sum of each row
   float* o_part;   // [2G][d / 4][256][4] unnormalised O, column-group major
@@ -150,7 +159,6 @@ struct BwdGrid {
   const int32_t* kv_len;
   const uint8_t* mask;  // block-sparse: uint8 [nt][nt], nonzero = (query tile, key tile) kept
   SplitPlan plan;
-  int* slot_item;   // split plans: [2G] tail item held by each slot, or -1
   float* dkv_part;  // split plans: [2G][2][d / 4][128][4] partial dV, dK (x scale)
 };
 
@@ -235,7 +243,8 @@ cudaError_t launch_fwd_plain(const FwdLaunch& a, const FwdGrid& g, int grid, cud
 cudaError_t launch_fwd_plain_dropout(const FwdLaunch& a, const FwdGrid& g, int grid,
                                      cudaStream_t stream);
 cudaError_t launch_fwd_sparse(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream);
-cudaError_t launch_fwd_split(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_split(const FwdLaunch& a, const FwdGrid& g, int grid, const MergeTable& m,
+                             cudaStream_t stream);
 // The backward main kernel's variants, one translation unit each: plain
 // (in fa_bwd.cu), sparse, plain with dropout, sparse with dropout, and split
 // (with or without dropout; with the merge kernel after it).
@@ -247,7 +256,7 @@ cudaError_t launch_bwd_main_dropout(const BwdLaunch& a, const BwdGrid& g, int gr
 cudaError_t launch_bwd_main_dropout_sparse(const BwdLaunch& a, const BwdGrid& g, int grid,
                                            cudaStream_t stream);
 cudaError_t launch_bwd_main_split(const BwdLaunch& a, const BwdGrid& g, int grid,
-                                  cudaStream_t stream);
+                                  const MergeTable& m, cudaStream_t stream);
 // Writes the keep decisions Z (1 = kept) of a.drop for [B*H, N, N] as bytes.
 cudaError_t launch_dropout_mask(const DropoutParams& drop, int BH, int N, uint8_t* keep,
                                 cudaStream_t stream);

@@ -180,6 +180,24 @@ static __device__ __noinline__ int list_window(TileSet ts, int w0, uint8_t* list
   return base;
 }
 
+// As list_window, for the union of two tile sets (the two Q tiles of a
+// forward item share their K/V loads).
+static __device__ __noinline__ int list_window2(TileSet a, TileSet b, int w0, uint8_t* list) {
+  const int lane = threadIdx.x & 31;
+  uint32_t ba[4], bb[4];
+  tile_window(a, w0, ba);
+  tile_window(b, w0, bb);
+  int base = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t u = ba[q] | bb[q];
+    if ((u >> lane) & 1u) list[base + __popc(u & ((1u << lane) - 1u))] = 32 * q + lane;
+    base += __popc(u);
+  }
+  __syncwarp();
+  return base;
+}
+
 // ------------------------------------------------------------------ item plan
 // Fewest tail steps a CTA is given: a part costs a partial-result write and
 // the merge a read of it, which a part of one or two steps would not repay.
@@ -197,10 +215,11 @@ __host__ __device__ __forceinline__ int plan_rounds(const SplitPlan& p, int G) {
   return p.whole < p.n_items ? p.whole / G : (p.n_items + G - 1) / G;
 }
 
-// Finds this CTA's tail range; steps(k) gives the steps of item k.
-// Warp-collective (one warp), about n_items - whole items scanned 32 at once.
+// Finds the tail range of CTA c of the split kernel (tail_ctas CTAs);
+// steps(k) gives the steps of item k. Warp-collective (one warp), the tail
+// items scanned 32 at once.
 template <typename StepsFn>
-__device__ TailRange tail_range(const SplitPlan& p, int c, int G, StepsFn steps) {
+__device__ TailRange tail_range(const SplitPlan& p, int c, StepsFn steps) {
   TailRange tr{0, 0, -1, 0};
   if (p.whole >= p.n_items || c >= p.tail_ctas) return tr;
   const long long s0 = p.tail * c / p.tail_ctas, s1 = p.tail * (c + 1) / p.tail_ctas;
@@ -244,25 +263,17 @@ struct Unit {
   int k, sb, se, slot;
 };
 
-// The r-th unit of CTA c (k = -1 when there is none). steps(k) as above.
-// `trp` points to the CTA's TailRange in shared memory; it is read afresh at
-// every call, so that callers short of registers do not keep it live.
+// The r-th tail unit of CTA c of the split kernel (k = -1 when there is
+// none). `trp` points to the CTA's TailRange in shared memory; it is read
+// afresh at every call, so that callers short of registers do not keep it
+// live. A cut item's part goes to slot 2c if it is the CTA's first tail
+// item, else to slot 2c + 1.
 template <typename StepsFn>
-__device__ __forceinline__ Unit unit_of(const SplitPlan& p, const TailRange* trp, int r, int c,
-                                        int G, StepsFn steps) {
+__device__ __forceinline__ Unit tail_unit(const TailRange* trp, int r, int c, StepsFn steps) {
   Unit u{-1, 0, 0, -1};
-  const int W = plan_rounds(p, G);
-  if (r < W) {
-    const int k = r * G + ((r & 1) ? G - 1 - c : c);
-    if (k < p.whole) {
-      u.k = k;
-      u.se = steps(k);
-    }
-    return u;
-  }
   const volatile TailRange* v = trp;
   const TailRange tr{v->t0, v->o0, v->t1, v->o1};
-  const int t = tr.t0 + (r - W);
+  const int t = tr.t0 + r;
   if (t > tr.t1) return u;
   const int n = steps(t);
   u.k = t;
@@ -272,61 +283,39 @@ __device__ __forceinline__ Unit unit_of(const SplitPlan& p, const TailRange* trp
   return u;
 }
 
-// Records which tail item (or -1) each of this CTA's two slots holds; n_first
-// and n_last are the steps of items tr.t0 and tr.t1. Only for split plans.
-__device__ __forceinline__ void write_slot_items(int* slot_item, const TailRange& tr, int c,
-                                                 int n_first, int n_last) {
-  int a = -1, b = -1;
-  if (tr.t1 >= tr.t0) {
-    if (tr.o0 > 0 || (tr.t1 == tr.t0 && tr.o1 < n_first)) a = tr.t0;
-    if (tr.t1 != tr.t0 && tr.o1 < n_last) b = tr.t1;
-  }
-  slot_item[2 * c] = a;
-  slot_item[2 * c + 1] = b;
-}
-
-// The slots holding parts of the item in slot s, if s is the first of them
-// (its owner): returns the number of slots and the last slot index; 0 when s
-// holds nothing or is not the owner. Parts of one item sit in slots that
-// follow each other, with at most unused (-1) slots between them.
-__device__ __forceinline__ int merge_slots(const int* slot_item, int n_slots, int s, int& s_last) {
-  const int t = slot_item[s];
-  if (t < 0) return 0;
-  for (int q = s - 1; q >= 0; --q) {
-    const int v = slot_item[q];
-    if (v == t) return 0;
-    if (v >= 0) break;
-  }
-  int n = 1;
-  s_last = s;
-  for (int q = s + 1; q < n_slots; ++q) {
-    const int v = slot_item[q];
-    if (v == t) {
-      ++n;
-      s_last = q;
-    } else if (v >= 0) {
-      break;
+// The merge table of a split plan, from the same arithmetic as tail_range
+// and tail_unit (host side).
+template <typename StepsFn>
+inline MergeTable build_merge_table(const SplitPlan& p, StepsFn steps) {
+  MergeTable m{};
+  m.n = 0;
+  m.first[0] = 0;
+  int np = 0, cur = -1;
+  int t = p.whole;
+  long long beg = 0;  // first tail step of item t
+  auto add = [&](int item, int slot) {
+    if (item != cur) {
+      m.item[m.n] = item;
+      m.first[m.n] = static_cast<short>(np);
+      ++m.n;
+      cur = item;
     }
+    m.slot[np++] = static_cast<short>(slot);
+    m.first[m.n] = static_cast<short>(np);
+  };
+  for (int c = 0; c < p.tail_ctas; ++c) {
+    const long long s0 = p.tail * c / p.tail_ctas, s1 = p.tail * (c + 1) / p.tail_ctas;
+    if (s1 <= s0) continue;
+    while (beg + steps(t) <= s0) beg += steps(t++);
+    const int t0 = t, o0 = static_cast<int>(s0 - beg);
+    int t1 = t;
+    long long b1 = beg;
+    while (b1 + steps(t1) <= s1 - 1) b1 += steps(t1++);
+    const int o1 = static_cast<int>(s1 - b1);
+    if (o0 > 0 || (t1 == t0 && o1 < steps(t0))) add(t0, 2 * c);
+    if (t1 != t0 && o1 < steps(t1)) add(t1, 2 * c + 1);
   }
-  return n;
-}
-
-// As list_window, for the union of two tile sets (the two Q tiles of a
-// forward item share their K/V loads).
-static __device__ __noinline__ int list_window2(TileSet a, TileSet b, int w0, uint8_t* list) {
-  const int lane = threadIdx.x & 31;
-  uint32_t ba[4], bb[4];
-  tile_window(a, w0, ba);
-  tile_window(b, w0, bb);
-  int base = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t u = ba[q] | bb[q];
-    if ((u >> lane) & 1u) list[base + __popc(u & ((1u << lane) - 1u))] = 32 * q + lane;
-    base += __popc(u);
-  }
-  __syncwarp();
-  return base;
+  return m;
 }
 
 // ------------------------------------------------------------------ item lists
@@ -408,6 +397,7 @@ inline SplitPlan plan_split(int n_items, int G, StepsFn steps, double item_cost,
   for (int k = W * G; k < n_items; ++k) T += steps(k);
   long long Gt = T / kMinTailSteps;
   if (Gt > G) Gt = G;
+  if (Gt > kMaxSplitCtas) Gt = kMaxSplitCtas;
   if (Gt < 1) Gt = 1;
   const double ms1 = whole_max + static_cast<double>(T) / Gt + 2.0 * (item_cost + part_cost) +
                      merge_cost;
@@ -419,25 +409,26 @@ inline SplitPlan plan_split(int n_items, int G, StepsFn steps, double item_cost,
 }
 
 
-// Split plans of the two passes on G CTAs. Costs in steps: every item costs
-// about one step of start-up (its first loads) and epilogue; a partial result
-// about one step to write; the merge kernel a few steps (it is a separate,
-// short launch). `allowed` is false when a workspace, key padding or a block
-// mask rules the split out.
+// Split plans of the two passes on G CTAs. Costs in steps (one K/V tile of
+// a forward item, one Q tile of a backward item), measured on GB300 by timing
+// launches with exactly one and two items per SM: the start-up and epilogue an
+// item adds beyond its steps (forward 2.6 steps at d = 128, 1 at d = 64;
+// backward 3 and 1.6), a partial result's write (about one step), and the
+// merge kernel with the extra launch of the split kernel. `allowed` is false
+// when a workspace, key padding or a block mask rules the split out.
 inline SplitPlan plan_fwd(int B, int H, int N, int d, bool causal, int G, bool allowed) {
   const int nqt = (N + 127) / 128, npairs = (nqt + 1) / 2, BH = B * H;
   const int n = BH * npairs;  // callers have checked that B H ceil(N / 128) fits in an int
   return plan_split(n, G,
-                    [&](int k) { return fwd_item_steps(nqt, npairs, BH, causal, k); }, 1.0, 1.0,
-                    d == 128 ? 2.0 : 4.0, allowed);
+                    [&](int k) { return fwd_item_steps(nqt, npairs, BH, causal, k); },
+                    d == 128 ? 2.6 : 1.0, 1.0, d == 128 ? 7.0 : 8.0, allowed);
 }
 
 inline SplitPlan plan_bwd(int B, int H, int N, int d, bool causal, int G, bool allowed) {
   const int nt = (N + 127) / 128, BH = B * H;
   const int n = BH * nt;
-  return plan_split(n, G,
-                    [&](int k) { return bwd_item_steps(nt, BH, causal, k); }, 1.0, 1.0,
-                    d == 128 ? 2.0 : 4.0, allowed);
+  return plan_split(n, G, [&](int k) { return bwd_item_steps(nt, BH, causal, k); },
+                    d == 128 ? 3.0 : 1.6, 1.0, d == 128 ? 3.5 : 5.0, allowed);
 }
 
 }  // namespace fa

@@ -55,18 +55,24 @@ def test_split_forward_few_problems(fa, d, causal, N):
 
 
 def test_split_forward_whole_wave_then_tail(fa):
-    """More items than SMs: a whole first wave, then a short tail of items cut
-    into parts of a few K/V tiles each (heads 0 and the last one checked)."""
+    """More items than SMs: a whole first wave on the plain kernel, then the
+    tail -- the last heads' items -- cut into parts on the split kernel. Rows
+    sampled across every Q tile of the first head (whole items) and of the
+    last head (cut items)."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    H = sms // 8 + 2  # pairs per head at N = 2048: 8; items = 8 H > sms
-    assert_fwd_split(fa, 1, H, 2048, 128, False)
-    w, x = inputs(1, H, 2048, 128, False, seed=5, backward=False)
+    N, d = 8192, 128
+    H = sms // 32 + 2  # 32 Q-tile pairs per head; items = 32 H > sms
+    assert_fwd_split(fa, 1, H, N, d, False)
+    w, x = inputs(1, H, N, d, False, seed=5, backward=False)
     o, lse = fa.forward(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), scale=w.scale)
     torch.cuda.synchronize()
     assert fa.device_status() == 0
     heads = [0, H - 1]
-    o_ref, l_ref = oracle.forward(x["q"][:, heads], x["k"][:, heads], x["v"][:, heads], w.scale)
-    check_fwd(f64(o)[:, heads], f64(lse)[:, heads], o_ref, l_ref, "wave + tail")
+    rows = np.arange(5, N, 61)
+    o_ref, l_ref = oracle.forward(x["q"][:, heads], x["k"][:, heads], x["v"][:, heads], w.scale,
+                                  rows=rows)
+    check_fwd(f64(o)[:, heads][:, :, rows], f64(lse)[:, heads][:, :, rows], o_ref, l_ref,
+              "wave + tail")
 
 
 def test_split_forward_workspace_contents_ignored(fa):
