@@ -39,8 +39,14 @@ cudaError_t launch_fwd(const FwdLaunch& a, cudaStream_t stream) {
         g.plan, [&](int k) { return fwd_item_steps(nqt, npairs, BH, causal, k); });
     return launch_fwd_split(a, g, g.plan.tail_ctas, m, stream);
   }
+  if (a.block_mask != nullptr) {
+    // d = 64: items pair the same Q tile of two heads, which keep the same
+    // block-mask row, so both Q slots visit every K/V step of the item.
+    if (a.d == 64) g.n_items = a.B * ((a.H + 1) / 2) * g.nqt;
+    g.plan = SplitPlan{g.n_items, g.n_items, 0, 0};  // every item whole
+    return launch_fwd_sparse(a, g, min(g.n_items, sms), stream);
+  }
   const int grid = min(g.n_items, sms);
-  if (a.block_mask != nullptr) return launch_fwd_sparse(a, g, grid, stream);
   if (a.drop.enabled) return launch_fwd_plain_dropout(a, g, grid, stream);
   return launch_fwd_plain(a, g, grid, stream);
 }

@@ -70,26 +70,37 @@ constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled c
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 
-template <int D>
+// kHP: items pair the same Q tile of two heads, each slot with a K/V ring
+// of its own (block-sparse at d = 64, where the two heads visit the same K/V
+// tiles); otherwise items pair adjacent Q tiles of one head, which share one
+// K/V ring.
+template <int D, bool kHP = false>
 struct FwdLayout {
   // d = 64 leaves TMEM room for P in columns of its own: the next S of a tile
   // can then be computed while the softmax of the current one still runs.
   static constexpr bool kSepP = (D == 64);
   static constexpr int kChunks = D / 64;
   static constexpr int kTile = kChunks * kChunk;  // one 128 x D bf16 tile
-  static constexpr int kKS = 3;                   // K ring slots
-  static constexpr int kVS = (D == 128) ? 2 : 3;  // V ring slots
+  static constexpr int kRings = kHP ? 2 : 1;      // K/V rings (one per Q slot with kHP)
+  static constexpr int kKS = kHP ? 2 : 3;         // K ring slots
+  static constexpr int kVS = kHP ? 2 : ((D == 128) ? 2 : 3);  // V ring slots
   static constexpr int kQS = (D == 128) ? 1 : 2;  // Q stages per tile slot
   static constexpr int kQ = 0;                    // Q of slot t, stage s: kQ + (t kQS + s) kTile
-  static constexpr int kK = kQ + 2 * kQS * kTile;
-  static constexpr int kV = kK + kKS * kTile;
-  static constexpr int kBar = kV + kVS * kTile;
-  static constexpr int kEnd = kBar + 512 + 8 * 128;  // barriers, TMEM address, abort flag, tail range; tile lists
+  static constexpr int kK = kQ + 2 * kQS * kTile; // K of ring x, slot s: kK + (x kKS + s) kTile
+  static constexpr int kV = kK + kRings * kKS * kTile;
+  static constexpr int kBar = kV + kRings * kVS * kTile;
+  // barriers, TMEM address, abort flag, tail range; then one 128-byte tile
+  // list per warp (at most 12 warps)
+  static constexpr int kEnd = kBar + 512 + 12 * 128;
   static constexpr int kSmem = kEnd + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t kTO = 256;       // O_A; O_B at kTO + D
   // P_t (bf16 pairs, 64 columns): its own columns, or over the first 64 of S_t
   static constexpr uint32_t kTP = kSepP ? 256 + 2 * D : 0;
   __host__ __device__ static constexpr uint32_t p_col(int t) { return kSepP ? kTP + t * 64 : t * 128; }
+  // barrier offsets (in 8-byte words from kBar)
+  static constexpr int oKF = 8, oKE = kHP ? 12 : 11, oVF = kHP ? 16 : 14, oVE = kHP ? 20 : 17;
+  static constexpr int oS = kHP ? 24 : 20;  // sfull [2], then pfull, odone, sfree, final [2 each]
+  static constexpr int oTmem = oS + 10, oAbort = oS + 11, oTail = oS + 12;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -124,7 +135,7 @@ __device__ __forceinline__ void bulk_wait_read0() {
 // K/V tiles [sb, se); `slot` >= 0 names the workspace slot its partial result
 // goes to (-1: the whole item, O and LSE written directly).
 struct FwdItem {
-  int k, bh, qtA, qtB, kv_bound, slot;
+  int k, bh, bhB, qtA, qtB, kv_bound, slot;  // bh, bhB: problems of Q tiles A and B
   TileSet tsA, tsB;
 };
 
@@ -133,15 +144,26 @@ __host__ __device__ __forceinline__ int fwd_steps(const FwdGrid& g, int k) {
   return fwd_item_steps(g.nqt, g.npairs, g.n_items / g.npairs, CAUSAL, k);
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool kHP = false>
 __device__ FwdItem make_item(const FwdGrid& g, const Unit& u) {
   FwdItem it;
-  int p;
-  fwd_item_coords(g.npairs, g.n_items / g.npairs, CAUSAL, u.k, it.bh, p);
   it.k = u.k;
   it.slot = u.slot;
-  it.qtA = 2 * p;
-  it.qtB = 2 * p + 1 < g.nqt ? 2 * p + 1 : -1;
+  if constexpr (kHP) {
+    // Q tile r of heads 2 hp and 2 hp + 1 of batch b: one mask row for both.
+    const int HP = (g.H + 1) / 2, bhp = u.k / g.nqt, r = u.k - bhp * g.nqt;
+    const int b = bhp / HP, hp = bhp - b * HP;
+    it.bh = b * g.H + 2 * hp;
+    it.bhB = 2 * hp + 1 < g.H ? it.bh + 1 : -1;
+    it.qtA = r;
+    it.qtB = it.bhB >= 0 ? r : -1;
+  } else {
+    int p;
+    fwd_item_coords(g.npairs, g.n_items / g.npairs, CAUSAL, u.k, it.bh, p);
+    it.bhB = it.bh;
+    it.qtA = 2 * p;
+    it.qtB = 2 * p + 1 < g.nqt ? 2 * p + 1 : -1;
+  }
   it.kv_bound = g.N;
   if (g.kv_len != nullptr) it.kv_bound = min(g.N, max(0, g.kv_len[it.bh / g.H]));
   const int kv_tiles = (it.kv_bound + kBlock - 1) / kBlock;
@@ -179,29 +201,34 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
                const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
                float* __restrict__ lse_out, FwdGrid g, float scale_log2, DropoutParams dp,
                int* status, long long wait_limit) {
-  using L = FwdLayout<D>;
+  // Block-sparse at d = 64: items pair one Q tile of two heads (same mask row),
+  // each Q slot with a K/V ring of its own.
+  constexpr bool kHP = (MODE == kModeSparse && D == 64);
+  using L = FwdLayout<D, kHP>;
   constexpr int KS = L::kKS, VS = L::kVS, QS = L::kQS;
   constexpr bool kSepP = L::kSepP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* bar_qfull = bars + 0;    // [2][QS] per Q slot (A, B) and stage
-  uint64_t* bar_qempty = bars + 4;   // [2][QS]
-  uint64_t* bar_kfull = bars + 8;    // [KS]
-  uint64_t* bar_kempty = bars + 11;  // [KS]
-  uint64_t* bar_vfull = bars + 14;   // [VS]
-  uint64_t* bar_vempty = bars + 17;  // [VS]
-  uint64_t* bar_sfull = bars + 20;   // [2]
-  uint64_t* bar_pfull = bars + 22;   // [2]
-  uint64_t* bar_odone = bars + 24;   // [2]
-  uint64_t* bar_sfree = bars + 26;   // [2] S_t read out of TMEM (separate-P layout)
-  uint64_t* bar_final = bars + 28;   // [2] one per MMA issuer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 30);
-  int* abort_flag = reinterpret_cast<int*>(bars + 31);
-  TailRange* tail_sh = reinterpret_cast<TailRange*>(bars + 32);  // this CTA's share of a split tail
+  uint64_t* bar_qfull = bars + 0;          // [2][QS] per Q slot (A, B) and stage
+  uint64_t* bar_qempty = bars + 4;         // [2][QS]
+  uint64_t* bar_kfull = bars + L::oKF;     // [rings][KS]
+  uint64_t* bar_kempty = bars + L::oKE;    // [rings][KS]
+  uint64_t* bar_vfull = bars + L::oVF;     // [rings][VS]
+  uint64_t* bar_vempty = bars + L::oVE;    // [rings][VS]
+  uint64_t* bar_sfull = bars + L::oS;      // [2]
+  uint64_t* bar_pfull = bars + L::oS + 2;  // [2]
+  uint64_t* bar_odone = bars + L::oS + 4;  // [2]
+  uint64_t* bar_sfree = bars + L::oS + 6;  // [2] S_t read out of TMEM (separate-P layout)
+  uint64_t* bar_final = bars + L::oS + 8;  // [2] one per MMA issuer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::oTmem);
+  int* abort_flag = reinterpret_cast<int*>(bars + L::oAbort);
+  TailRange* tail_sh = reinterpret_cast<TailRange*>(bars + L::oTail);  // this CTA's share of a split tail
   uint8_t* walk_list = reinterpret_cast<uint8_t*>(bars + 64);     // [warp][128] kept tiles of a window (sparse)
   constexpr int kMmaB = FwdWarps<D>::kMmaB, kSoft0 = FwdWarps<D>::kSoft0;
-  constexpr int kIssuers = kSepP ? 2 : 1;  // arrivals that release a K or V ring slot
+  // arrivals that release a K or V ring slot: both issuers at d = 64 when the
+  // slots share one ring, else the one issuer that uses it
+  constexpr int kIssuers = (kSepP && !kHP) ? 2 : 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -217,11 +244,11 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       mbar_init(bar_odone + t, 1);
       mbar_init(bar_sfree + t, 4);
     }
-    for (int s = 0; s < KS; ++s) {
+    for (int s = 0; s < L::kRings * KS; ++s) {
       mbar_init(bar_kfull + s, 1);
       mbar_init(bar_kempty + s, kIssuers);
     }
-    for (int s = 0; s < VS; ++s) {
+    for (int s = 0; s < L::kRings * VS; ++s) {
       mbar_init(bar_vfull + s, 1);
       mbar_init(bar_vempty + s, kIssuers);
     }
@@ -277,6 +304,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     int nqA = 0, nqB = 0;  // Q loads issued per slot
     int k_issued = 0, v_issued = 0;
     int u = 0;           // position in the K/V rings, continued across items
+    int uB = 0, kB_issued = 0, vB_issued = 0;  // ring B (head-paired items)
     bool ok = true;
     // Q loads of a unit's two tiles (lane 0); false on an abort.
     auto load_q = [&](const FwdItem& it, int lastA, int lastB) -> bool {
@@ -289,36 +317,66 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         mbar_expect_tx(bar_qfull + qb, L::kTile);
         for (int c = 0; c < L::kChunks; ++c)
           tma_load_rows(smem + L::kQ + qb * L::kTile + c * kChunk, &tm_q, bar_qfull + qb, c * 64,
-                        (t ? it.qtB : it.qtA) * kBlock, it.bh, g.H, g.st);
+                        (t ? it.qtB : it.qtA) * kBlock, kHP ? (t ? it.bhB : it.bh) : it.bh, g.H,
+                        g.st);
         ++nq;
       }
       return true;
     };
-    // K_j and V_j into the next ring position (lane 0); false on an abort.
-    auto load_kv = [&](const FwdItem& it, int j) -> bool {
-      const int ks = u % KS, vs = u % VS;
-      if (u >= KS && !mbar_wait(bar_kempty + ks, ((u / KS) - 1) & 1, wd)) return false;
+    // K_j and V_j of problem bh into the next position uu of K/V ring `ring`
+    // (lane 0); false on an abort.
+    auto load_kv_r = [&](int ring, int bh, int j, int& uu, int& ki, int& vi) -> bool {
+      const int ks = ring * KS + uu % KS, vs = ring * VS + uu % VS;
+      if (uu >= KS && !mbar_wait(bar_kempty + ks, ((uu / KS) - 1) & 1, wd)) return false;
       mbar_expect_tx(bar_kfull + ks, L::kTile);
       for (int c = 0; c < L::kChunks; ++c)
         tma_load_rows(smem + L::kK + ks * L::kTile + c * kChunk, &tm_k, bar_kfull + ks, c * 64,
-                      j * kBlock, it.bh, g.H, g.st);
-      k_issued = u + 1;
-      if (u >= VS && !mbar_wait(bar_vempty + vs, ((u / VS) - 1) & 1, wd)) return false;
+                      j * kBlock, bh, g.H, g.st);
+      ki = uu + 1;
+      if (uu >= VS && !mbar_wait(bar_vempty + vs, ((uu / VS) - 1) & 1, wd)) return false;
       mbar_expect_tx(bar_vfull + vs, L::kTile);
       for (int c = 0; c < L::kChunks; ++c)
         tma_load_rows(smem + L::kV + vs * L::kTile + c * kChunk, &tm_v, bar_vfull + vs, c * 64,
-                      j * kBlock, it.bh, g.H, g.st);
-      v_issued = u + 1;
-      ++u;
+                      j * kBlock, bh, g.H, g.st);
+      vi = uu + 1;
+      ++uu;
       return true;
     };
-    if constexpr (MODE == kModeSparse) {
+    auto load_kv = [&](const FwdItem& it, int j) -> bool {
+      return load_kv_r(0, it.bh, j, u, k_issued, v_issued);
+    };
+    if constexpr (kHP) {
+      // Head-paired items: both Q tiles keep the same mask row. The whole warp
+      // lists each 128-tile window's kept tiles; lane 0 loads each tile's K and
+      // V of head A into ring A and of head B into ring B.
+      for (int r = 0; ok; ++r) {
+        const Unit un = unit(r);
+        if (un.k < 0) break;
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un);
+        TileWalk<> wa;
+        wa.init(it.tsA);
+        const int lastA = wa.last(), lastB = it.bhB >= 0 ? lastA : -1;
+        if (lane == 0) ok = load_q(it, lastA, lastB);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        for (int w0 = it.tsA.begin & ~127; ok && w0 < it.tsA.end; w0 += 128) {
+          const int cnt = list_window(it.tsA, w0, list);
+          if (lane == 0) {
+            for (int idx = 0; ok && idx < cnt; ++idx) {
+              const int j = w0 + list[idx];
+              ok = load_kv_r(0, it.bh, j, u, k_issued, v_issued);
+              if (ok && it.bhB >= 0) ok = load_kv_r(1, it.bhB, j, uB, kB_issued, vB_issued);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        }
+      }
+    } else if constexpr (MODE == kModeSparse) {
       // The whole warp lists each 128-tile window's tiles (union of the two Q
       // tiles' mask rows); lane 0 then issues their copies.
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const FwdItem it = make_item<CAUSAL>(g, un);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un);
         TileWalk<> wa, wb;
         wa.init(it.tsA);
         wb.init(it.tsB);
@@ -338,7 +396,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const FwdItem it = make_item<CAUSAL>(g, un);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un);
         const int lastA = it.tsA.end > it.tsA.begin ? it.tsA.end - 1 : -1;
         const int lastB = it.tsB.end > it.tsB.begin ? it.tsB.end - 1 : -1;
         ok = load_q(it, lastA, lastB);
@@ -357,6 +415,12 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         mbar_wait_drain(bar_kfull + (t % KS), (t / KS) & 1, wait_limit);
       for (int t = max(0, v_issued - VS); t < v_issued; ++t)
         mbar_wait_drain(bar_vfull + (t % VS), (t / VS) & 1, wait_limit);
+      if constexpr (kHP) {
+        for (int t = max(0, kB_issued - KS); t < kB_issued; ++t)
+          mbar_wait_drain(bar_kfull + KS + (t % KS), (t / KS) & 1, wait_limit);
+        for (int t = max(0, vB_issued - VS); t < vB_issued; ++t)
+          mbar_wait_drain(bar_vfull + VS + (t % VS), (t / VS) & 1, wait_limit);
+      }
     }
     __syncwarp();
   } else if (warp == kMmaWarp || warp == kMmaB) {
@@ -372,11 +436,20 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       // commit when slot X used the tile, else with a plain arrive once the
       // tile is known to be loaded, which keeps the ring's phases in order.
       const int X = (warp == kMmaWarp) ? 0 : 1;
+      // With head-paired items slot X has K/V ring X and walks only its own
+      // tiles; otherwise both walk the shared ring (see above).
+      const int ring = kHP ? X : 0;
+      uint64_t* const kfull = bar_kfull + ring * KS;
+      uint64_t* const kempty = bar_kempty + ring * KS;
+      uint64_t* const vfull = bar_vfull + ring * VS;
+      uint64_t* const vempty = bar_vempty + ring * VS;
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);  // Q, K both K-major
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);     // P (TMEM), V MN-major
       const uint64_t q_desc = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);     // K-major
-      const uint64_t k_desc = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);     // K-major
-      const uint64_t v_desc = sdesc_sw128(smem_u32(smem + L::kV), kChunk, 1024);  // MN-major
+      const uint64_t k_desc =
+          sdesc_sw128(smem_u32(smem + L::kK + ring * KS * L::kTile), 16, 1024);   // K-major
+      const uint64_t v_desc =
+          sdesc_sw128(smem_u32(smem + L::kV + ring * VS * L::kTile), kChunk, 1024);  // MN-major
       const uint32_t s_tm = tmem + X * 128, o_tm = tmem + L::kTO + X * D;
       const uint32_t p_tm = tmem + L::p_col(X);
       uint64_t* my_sfull = bar_sfull + X;
@@ -389,27 +462,30 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       bool ok = true;
       auto k_wait = [&](int uu) -> bool {
         if (uu == k_ready) return true;
-        if (!mbar_wait_spin_w(bar_kfull + (uu % KS), (uu / KS) & 1, wd)) return false;
+        if (!mbar_wait_spin_w(kfull + (uu % KS), (uu / KS) & 1, wd)) return false;
         k_ready = uu;
         return true;
       };
       auto v_wait = [&](int uu) -> bool {
         if (uu == v_ready) return true;
-        if (!mbar_wait_spin_w(bar_vfull + (uu % VS), (uu / VS) & 1, wd)) return false;
+        if (!mbar_wait_spin_w(vfull + (uu % VS), (uu / VS) & 1, wd)) return false;
         v_ready = uu;
         return true;
       };
       for (int r = 0; ok; ++r) {
         const Unit un0 = unit(r);
         if (un0.k < 0) break;
-        const FwdItem it = make_item<CAUSAL>(g, un0);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un0);
         TileWalk<> wa, wb;  // block-mask walks (sparse)
         wa.init(it.tsA);
         wb.init(it.tsB);
         const int uend = max(it.tsA.end, it.tsB.end);
         // The next K/V tile >= j of the item and whether Q tiles A, B visit it.
         auto nxt = [&](int j, bool& hA, bool& hB) -> int {
-          if constexpr (MODE == kModeSparse) {
+          if constexpr (kHP) {  // only this slot's tiles, all of them its own
+            hA = hB = true;
+            return (X ? wb : wa).seek(j);
+          } else if constexpr (MODE == kModeSparse) {
             return next_pair_tile(wa, wb, j, hA, hB);
           } else {
             hA = j < it.tsA.end;
@@ -468,20 +544,20 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         };
         auto release_k = [&](int uu, bool used) -> bool {
           if (used) {
-            mma_commit_w(bar_kempty + (uu % KS));
+            mma_commit_w(kempty + (uu % KS));
             return true;
           }
           if (!k_wait(uu)) return false;
-          mbar_arrive_w(bar_kempty + (uu % KS));
+          mbar_arrive_w(kempty + (uu % KS));
           return true;
         };
         auto release_v = [&](int uu, bool used) -> bool {
           if (used) {
-            mma_commit_w(bar_vempty + (uu % VS));
+            mma_commit_w(vempty + (uu % VS));
             return true;
           }
           if (!v_wait(uu)) return false;
-          mbar_arrive_w(bar_vempty + (uu % VS));
+          mbar_arrive_w(vempty + (uu % VS));
           return true;
         };
         bool jA, jB;
@@ -535,7 +611,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un0 = unit(r);
         if (un0.k < 0) break;
-        const FwdItem it = make_item<CAUSAL>(g, un0);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un0);
         TileWalk<> wa, wb;  // block-mask walks (sparse)
         wa.init(it.tsA);
         wb.init(it.tsB);
@@ -663,12 +739,13 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     for (int ri = 0; ok; ++ri) {
       const Unit un0 = unit(ri);
       if (un0.k < 0) break;
-      const FwdItem it = make_item<CAUSAL>(g, un0);
+      const FwdItem it = make_item<CAUSAL, kHP>(g, un0);
       const int qt = t ? it.qtB : it.qtA;
       if (qt < 0) continue;
       const int jbeg = t ? it.tsB.begin : it.tsA.begin, jend = t ? it.tsB.end : it.tsA.end;
       const int kv_bound = it.kv_bound;
       const int row = qt * kBlock + r;
+      const int bh = kHP ? (t ? it.bhB : it.bh) : it.bh;  // this slot's (batch, head)
       float m = -INFINITY;  // reference max, log2 units (scale folded in)
       float l = 0.f;        // sum of exp2(s * scale_log2 - m) over visited keys
       int n = 0;            // tiles of this item
@@ -741,8 +818,8 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
           if constexpr (DROP) {
             // keys j*128 + 2*c0 + [0, 32): two Philox blocks of 16 keep bytes
             const uint32_t grp = static_cast<uint32_t>(j * kBlock + 2 * c0) >> 4;
-            const uint4 ra = philox4x32_10(grp, row, it.bh, dp.offset, dp.k0, dp.k1);
-            const uint4 rb = philox4x32_10(grp + 1, row, it.bh, dp.offset, dp.k0, dp.k1);
+            const uint4 ra = philox4x32_10(grp, row, bh, dp.offset, dp.k0, dp.k1);
+            const uint4 rb = philox4x32_10(grp + 1, row, bh, dp.offset, dp.k0, dp.k1);
             const uint32_t km[8] = {keep_bytes(ra.x, dp.thresh4), keep_bytes(ra.y, dp.thresh4),
                                     keep_bytes(ra.z, dp.thresh4), keep_bytes(ra.w, dp.thresh4),
                                     keep_bytes(rb.x, dp.thresh4), keep_bytes(rb.y, dp.thresh4),
@@ -837,7 +914,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       const bool live = have && l > 0.f;
       const float inv = live ? (DROP ? dp.rescale : 1.f) / l : 0.f;
       const bool row_ok = row < g.N;
-      uint4* orow = reinterpret_cast<uint4*>(out + row_offset(g.st, g.H, it.bh, row));
+      uint4* orow = reinterpret_cast<uint4*>(out + row_offset(g.st, g.H, bh, row));
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
         uint32_t o[32];
@@ -862,7 +939,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         }
       }
       if (row_ok)
-        lse_out[static_cast<size_t>(it.bh) * g.N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
+        lse_out[static_cast<size_t>(bh) * g.N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -940,7 +1017,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(FwdGrid g, const __grid_
 // Launches fwd_kernel<D, CAUSAL, DROP, MODE> on `grid` CTAs.
 template <int D, bool CAUSAL, bool DROP, int MODE>
 cudaError_t launch_fwd_kernel(const FwdLaunch& a, const FwdGrid& g, int grid, cudaStream_t stream) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, MODE == kModeSparse && D == 64>;
   auto kern = fwd_kernel<D, CAUSAL, DROP, MODE>;
   static std::atomic<unsigned long long> smem_set{0};
   cudaError_t e = set_smem_once(smem_set, reinterpret_cast<const void*>(kern), L::kSmem);
