@@ -411,6 +411,8 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
                  !encode_rows(&a.tm_k, p.k, B, H, N, d, lay) ||
                  !encode_rows(&a.tm_v, p.v, B, H, N, d, lay) ||
                  !encode_rows(&a.tm_do, p.dout, B, H, N, d, lay) ||
+                 !encode_rows(&a.tm_dk, p.dk, B, H, N, d, lay) ||
+                 !encode_rows(&a.tm_dv, p.dv, B, H, N, d, lay) ||
                  !encode_f32_rows(&a.tm_dqacc, wsb + ws.dq_off, B * H, npad, d)))
     return FA_ERR_CUDA;
   a.st = lay;

@@ -84,20 +84,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const 
       "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
-                                             int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 
 // ----------------------------------------------------------------- preprocess
 template <int D>
@@ -279,7 +265,8 @@ template <int D, bool CAUSAL, int MODE, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dqacc, __nv_bfloat16* __restrict__ dk,
+                    const __grid_constant__ CUtensorMap tm_dqacc, const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, const float* __restrict__ lse2,
                     const float* __restrict__ delta, BwdGrid grid, int Npad, float scale,
                     DropoutParams dp, int* status, long long wait_limit) {
@@ -668,42 +655,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // dV (x1) and dK (x scale) of the item, straight from TMEM rows to HBM;
-      // each accumulator is released as soon as it has been read.
+      // dV (x1, or x 1 / (1 - p') with dropout) and dK (x scale) of the item,
+      // 64 columns at a time: each accumulator is released as soon as it has
+      // been read out of TMEM. At d = 64 the bf16 chunk is staged in the dQ
+      // staging buffer (128-byte swizzle, free again after the last dQ round)
+      // and one TMA store writes it -- whole 128-byte rows in full sectors,
+      // rows past N clipped. Parts of split items write fp32 to their slot.
       if (!mbar_wait_warp(bar_accfull, t & 1, wd)) break;
       tc_fence_after();
+      constexpr int kHalf = D / 64, kOut = 2 * kHalf;  // chunks of dV, then of dK
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? L::kTDV : L::kTDK;
+      for (int oc = 0; oc < kOut; ++oc) {
+        const int which = oc / kHalf, h = oc % kHalf;
+        const uint32_t col = (which == 0 ? L::kTDV : L::kTDK) + h * 64;
         const float mul = which == 0 ? (DROP ? dp.rescale : 1.f) : scale;
-        uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + out_off);
+        uint32_t a[2][32];
+        tmem_ld32(lane_base + col, a[0]);
+        tmem_ld32(lane_base + col + 32, a[1]);
+        tmem_wait_ld();
+        reg_fence(a[0]);
+        reg_fence(a[1]);
+        if (h == kHalf - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(which == 0 ? bar_dvempty : bar_dkempty);
+        }
+        if (MODE == kModeSplit && x.slot >= 0) {
+          // Part of a split item: fp32 into its workspace slot, column-group
+          // major ([slot][dV, dK][D / 4][128 rows][4 floats]), so that the
+          // 32 rows of a warp write 512 contiguous bytes per store.
+          float4* part = reinterpret_cast<float4*>(grid.dkv_part) +
+                         (static_cast<size_t>(x.slot) * 2 + which) * (D / 4) * kBlock + row;
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          uint32_t a[2][32];
-          tmem_ld32(lane_base + col + h * 64, a[0]);
-          tmem_ld32(lane_base + col + h * 64 + 32, a[1]);
-          tmem_wait_ld();
-          reg_fence(a[0]);
-          reg_fence(a[1]);
-          if (h == D / 64 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(which == 0 ? bar_dvempty : bar_dkempty);
+          for (int u = 0; u < 16; ++u) {
+            const uint32_t* s = &a[u >> 3][(u & 7) * 4];
+            part[(h * 16 + u) * kBlock] =
+                make_float4(__uint_as_float(s[0]) * mul, __uint_as_float(s[1]) * mul,
+                            __uint_as_float(s[2]) * mul, __uint_as_float(s[3]) * mul);
           }
-          if (MODE == kModeSplit && x.slot >= 0) {
-            // Part of a split item: fp32 into its workspace slot, column-group
-            // major ([slot][dK, dV][D / 4][128 rows][4 floats]), so that the
-            // 32 rows of a warp write 512 contiguous bytes per store.
-            float4* part = reinterpret_cast<float4*>(grid.dkv_part) +
-                           (static_cast<size_t>(x.slot) * 2 + which) * (D / 4) * kBlock + row;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-              const uint32_t* s = &a[u >> 3][(u & 7) * 4];
-              part[(h * 16 + u) * kBlock] =
-                  make_float4(__uint_as_float(s[0]) * mul, __uint_as_float(s[1]) * mul,
-                              __uint_as_float(s[2]) * mul, __uint_as_float(s[3]) * mul);
-            }
-          } else if (key < N) {
+          continue;
+        }
+        if constexpr (D == 128) {
+          // d = 128: straight from the registers to global memory, one row
+          // per thread. (The staged path below costs this variant more in
+          // the registers its dQ drain already keeps at the limit than the
+          // stores gain.)
+          if (key < N) {
+            uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + out_off);
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               const uint32_t* s = &a[u >> 2][(u & 3) * 8];
@@ -714,10 +712,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                   pack_bf16(__uint_as_float(s[6]) * mul, __uint_as_float(s[7]) * mul));
             }
           }
+          continue;
+        }
+        const int cc = oc % L::kDQChunks;  // staging chunk of this output chunk
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t* s = &a[u >> 2][(u & 3) * 8];
+          st_shared_v4(st_base + cc * kChunk + row * 128 + ((u ^ (row & 7)) << 4),
+                       pack_bf16(__uint_as_float(s[0]) * mul, __uint_as_float(s[1]) * mul),
+                       pack_bf16(__uint_as_float(s[2]) * mul, __uint_as_float(s[3]) * mul),
+                       pack_bf16(__uint_as_float(s[4]) * mul, __uint_as_float(s[5]) * mul),
+                       pack_bf16(__uint_as_float(s[6]) * mul, __uint_as_float(s[7]) * mul));
+        }
+        if (cc == L::kDQChunks - 1 || oc == kOut - 1) {  // staging full, or the last chunk
+          fence_proxy_async_smem();
+          named_bar_sync(3, 128);
+          if (issuer) {
+#pragma unroll
+            for (int c2 = 0; c2 <= cc; ++c2) {
+              const int o2 = oc - cc + c2;
+              tma_store_rows(o2 < kHalf ? &tm_dv : &tm_dk, stage + c2 * kChunk, (o2 % kHalf) * 64,
+                             x.j * kBlock, x.bh, grid.H, grid.st);
+            }
+            bulk_commit();
+            bulk_wait_read0();
+          }
+          named_bar_sync(3, 128);
         }
       }
       ++t;
     }
+    if (issuer) bulk_wait0();  // every dQ reduction and dK / dV store has completed
   } else {
     // ------------------------------------------------------------ P / dS (warps 0-7)
     const int wg = warp >> 2;             // query columns [64 wg, 64 wg + 64)
@@ -913,7 +938,8 @@ cudaError_t launch_bwd_main_kernel(const BwdLaunch& a, const BwdGrid& g, int gri
   cudaError_t e = set_smem_once(smem_set, reinterpret_cast<const void*>(kern), L::kSmem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), L::kSmem, stream, a.tm_q, a.tm_k, a.tm_v,
-                    a.tm_do, a.tm_dqacc, a.dk, a.dv, a.lse2, a.delta, g, g.nt * kBlock, a.scale,
+                    a.tm_do, a.tm_dqacc, a.tm_dk, a.tm_dv, a.dk, a.dv, a.lse2, a.delta, g,
+                    g.nt * kBlock, a.scale,
                     a.drop, a.status, a.wait_limit);
 }
 

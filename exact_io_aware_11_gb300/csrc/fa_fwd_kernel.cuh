@@ -114,20 +114,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return m;
 }
 
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
-                                             int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read0() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 
 // One work unit: Q tiles 2p and 2p+1 (qtB = -1 if absent) of one (batch,
 // head), restricted to the K/V steps [sb, se) of the unit. Without a block

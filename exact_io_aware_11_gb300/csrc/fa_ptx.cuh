@@ -222,6 +222,49 @@ __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map,
   }
 }
 
+// 3-D / 4-D tiled stores shared -> global (bulk-group completion), the
+// counterparts of the loads above: whole 128-byte rows leave in full sectors,
+// and rows beyond the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int x, int y,
+                                             int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+// 128 rows (from `row`) x 64 columns (from `x`) of problem bh of a [B, H, N, d]
+// tensor map, from a 128-byte-swizzled shared-memory chunk.
+__device__ __forceinline__ void tma_store_rows(const CUtensorMap* map, const void* src, int x, int row,
+                                               int bh, int H, const Strides& st) {
+  if (st.merged) {
+    tma_store_3d(map, src, x, row, bh);
+  } else {
+    int y0, y1, y2;
+    row_coords(st, row, bh % H, bh / H, y0, y1, y2);
+    tma_store_4d(map, src, x, y0, y1, y2);
+  }
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The shared-memory sources of every committed bulk group have been read.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed bulk group has completed (its global writes performed).
+__device__ __forceinline__ void bulk_wait0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
