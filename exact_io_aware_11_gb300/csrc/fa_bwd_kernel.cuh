@@ -772,6 +772,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = gq % QS;
         const float* st_lse = reinterpret_cast<const float*>(smem + L::kStat + s * 1024) + qc0;
         const float* st_delta = st_lse + 128;
+        // Keep decisions of key kr against query columns qc0 + 32 h + e in
+        // kb[h] (keep_bits32 layout). They do not depend on S, so they are
+        // drawn before S^T is awaited, filling the wait for the MMA.
+        uint32_t kb[2] = {~0u, ~0u};
+        if constexpr (DROP) {
+          // Lane (half h = lane / 16, p = lane % 16) draws the Philox blocks of
+          // queries qc0 + 16 r + p (r = 0..3) for its half-warp's 16-key group;
+          // a byte transpose across the half-warp leaves each lane the bytes of
+          // its own key kr: byte b of kw[r][w] is query qc0 + 16 r + 4 w + b.
+          const uint32_t c4 = 0x80808080u - (dp.thresh4 & 0x7f7f7f7fu);
+          const uint32_t grp = static_cast<uint32_t>(x.j * kBlock + quarter * 32 + (lane & 16)) >> 4;
+          const uint32_t qrow = static_cast<uint32_t>(i * kBlock + qc0 + (lane & 15));
+          uint32_t kw[4][4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const uint4 v4 = philox4x32_10(grp, qrow + 16 * r, x.bh, dp.offset, dp.k0, dp.k1);
+            kw[r][0] = v4.x;
+            kw[r][1] = v4.y;
+            kw[r][2] = v4.z;
+            kw[r][3] = v4.w;
+            transpose16_bytes(kw[r], lane);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            kb[h] = keep_bits32(make_uint4(kw[2 * h][0], kw[2 * h][1], kw[2 * h][2], kw[2 * h][3]),
+                                make_uint4(kw[2 * h + 1][0], kw[2 * h + 1][1], kw[2 * h + 1][2],
+                                           kw[2 * h + 1][3]),
+                                dp.thresh4, c4);
+          asm volatile("" : "+r"(kb[0]), "+r"(kb[1]));
+        }
         if (!mbar_wait_warp(bar_qfull + s, (gq / QS) & 1, wd)) { ok = false; break; }
         if (!mbar_wait_warp(bar_sfull, gq & 1, wd)) { ok = false; break; }
         tc_fence_after();
@@ -802,33 +832,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[c / 2 + 1] = key_live ? pack_bf16(p2, p3) : 0u;
         }
         // P^T over the first 32 of this warpgroup's 64 S^T columns (already read)
-        uint32_t kbits[2] = {~0u, ~0u};  // keep bit of query column c: kbits[c / 32] bit c % 32
         if constexpr (DROP) {
-          // Lane (half h = lane / 16, p = lane % 16) draws the Philox blocks of
-          // queries qc0 + 16 r + p (r = 0..3) for its half-warp's 16-key group;
-          // a byte transpose across the half-warp leaves each lane the bytes of
-          // its own key kr: byte b of kw[r][w] is query qc0 + 16 r + 4 w + b.
-          const uint32_t grp = static_cast<uint32_t>(x.j * kBlock + quarter * 32 + (lane & 16)) >> 4;
-          const uint32_t qrow = static_cast<uint32_t>(i * kBlock + qc0 + (lane & 15));
-          uint32_t km[16];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const uint4 v4 = philox4x32_10(grp, qrow + 16 * r, x.bh, dp.offset, dp.k0, dp.k1);
-            uint32_t kw[4] = {v4.x, v4.y, v4.z, v4.w};
-            transpose16_bytes(kw, lane);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) km[4 * r + w] = keep_bytes(kw[w], dp.thresh4);
-          }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t pd[16];  // dropped P^T pairs (query columns 32 h + 2 c, + 1)
 #pragma unroll
-            for (int c = 0; c < 16; ++c) pd[c] = pk[16 * h + c] & pair_mask(km[8 * h + (c >> 1)], c & 1);
+            for (int c = 0; c < 16; ++c) pd[c] = pk[16 * h + c] & pair_mask_bits(kb[h], c);
             tmem_st16(lane_base + L::kTS + qc0 + 16 * h, pd);
-            uint32_t b = 0;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) b |= keep_nibble(km[8 * h + w]) << (4 * w);
-            kbits[h] = b;
           }
         } else {
           tmem_st32(lane_base + L::kTS + qc0, pk);
@@ -864,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
             float dpe = __uint_as_float(rr[(q0 + e) >> 5][(q0 + e) & 31]);
             if constexpr (DROP)
-              dpe = ((kbits[(q0 + e) >> 5] >> ((q0 + e) & 31)) & 1u) ? dpe * dp.rescale : 0.f;
+              dpe = keep_bit(kb[(q0 + e) >> 5], (q0 + e) & 31) ? dpe * dp.rescale : 0.f;
             gv[e] = pe * (dpe - dd[e]);
           }
           const uint32_t addr = ds_base + kr * 128 + (((u ^ (kr & 7))) << 4);

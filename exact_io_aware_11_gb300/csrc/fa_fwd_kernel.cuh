@@ -738,6 +738,22 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       // One K/V tile j of this slot: S_t(j) from TMEM, the online softmax
       // update, P_t(j) to TMEM, then pfull. False when the CTA is aborting.
       auto tile = [&](const int j) -> bool {
+        // Keep decisions of this row's 128 keys, one word per 32 keys
+        // (keep_bits32). They do not depend on S, so they are drawn before
+        // S_t(j) is awaited: the draws fill the wait for the MMA instead of
+        // lengthening the softmax, which the next MMA waits for.
+        uint32_t kb[4] = {0u, 0u, 0u, 0u};
+        if constexpr (DROP) {
+          const uint32_t c4 = 0x80808080u - (dp.thresh4 & 0x7f7f7f7fu);
+          const uint32_t g0 = static_cast<uint32_t>(j * kBlock) >> 4;  // 16-key group of key j*128
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 ra = philox4x32_10(g0 + 2 * q, row, bh, dp.offset, dp.k0, dp.k1);
+            const uint4 rb = philox4x32_10(g0 + 2 * q + 1, row, bh, dp.offset, dp.k0, dp.k1);
+            kb[q] = keep_bits32(ra, rb, dp.thresh4, c4);
+          }
+          asm volatile("" : "+r"(kb[0]), "+r"(kb[1]), "+r"(kb[2]), "+r"(kb[3]));
+        }
         if (!mbar_wait_warp<true>(bar_sfull + t, ns & 1, wd)) {
           return false;
         }
@@ -801,17 +817,9 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
             pk[c] = pack_bf16(p0, p1);
             ps[c & 3] += p0 + p1;
           }
-          if constexpr (DROP) {
-            // keys j*128 + 2*c0 + [0, 32): two Philox blocks of 16 keep bytes
-            const uint32_t grp = static_cast<uint32_t>(j * kBlock + 2 * c0) >> 4;
-            const uint4 ra = philox4x32_10(grp, row, bh, dp.offset, dp.k0, dp.k1);
-            const uint4 rb = philox4x32_10(grp + 1, row, bh, dp.offset, dp.k0, dp.k1);
-            const uint32_t km[8] = {keep_bytes(ra.x, dp.thresh4), keep_bytes(ra.y, dp.thresh4),
-                                    keep_bytes(ra.z, dp.thresh4), keep_bytes(ra.w, dp.thresh4),
-                                    keep_bytes(rb.x, dp.thresh4), keep_bytes(rb.y, dp.thresh4),
-                                    keep_bytes(rb.z, dp.thresh4), keep_bytes(rb.w, dp.thresh4)};
+          if constexpr (DROP) {  // keys j*128 + 2*c0 + [0, 32)
 #pragma unroll
-            for (int c = 0; c < 16; ++c) pk[c] &= pair_mask(km[c >> 1], c & 1);
+            for (int c = 0; c < 16; ++c) pk[c] &= pair_mask_bits(kb[c0 >> 4], c);
           }
           tmem_st16(lane_base + p_col + c0, pk);
         }

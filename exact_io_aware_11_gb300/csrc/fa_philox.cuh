@@ -38,13 +38,43 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
   return make_uint4(c0, c1, c2, c3);
 }
 
-// 0xff in each byte of `w` that is >= the byte threshold (replicated in t4), else 0x00.
-__device__ __forceinline__ uint32_t keep_bytes(uint32_t w, uint32_t t4) { return __vcmpgeu4(w, t4); }
+// Sign bit of each byte of the result = [byte of w >= byte of t4] (t4: the
+// threshold replicated into the four bytes); the other bits are garbage.
+// c4 = 0x80808080 - (t4 & 0x7f7f7f7f). Bytes are compared without carries
+// between them: (w & 0x7f) + 0x80 - (t & 0x7f) has its top bit set iff the
+// low seven bits of w are >= those of t, which decides where the top bits of
+// w and t agree; where they differ, the top bit of w decides.
+__device__ __forceinline__ uint32_t keep_msb(uint32_t w, uint32_t t4, uint32_t c4) {
+  const uint32_t d = (w & 0x7f7f7f7fu) + c4;
+  return (w & ~t4) | (~(w ^ t4) & d);
+}
 
-// For a pair of elements whose keep bytes are bytes (2 s, 2 s + 1) of `m`
-// (s = 0 or 1): a mask that clears the dropped bf16 halves of a packed pair.
-__device__ __forceinline__ uint32_t pair_mask(uint32_t m, int s) {
-  return __byte_perm(m, 0u, s ? 0x3322u : 0x1100u);
+// The keep decisions of 32 consecutive keys (two Philox blocks: key e takes
+// byte e mod 4 of word e / 4 of {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w}) in
+// one word: key e = 4 w + b at bit 8 b + 7 - w, so that shifting the word
+// left by w brings the decisions of keys 4 w .. 4 w + 3 to the sign bits of
+// bytes 0..3.
+__device__ __forceinline__ uint32_t keep_bits32(const uint4& a, const uint4& b, uint32_t t4, uint32_t c4) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r |= (keep_msb(w[i], t4, c4) & 0x80808080u) >> i;
+  return r;
+}
+
+// Mask for the packed bf16 pair of keys (2 c, 2 c + 1), c = 0..15, of a word
+// made by keep_bits32: 0xffff over each kept half, 0 over a dropped one
+// (prmt with the sign-replicating selector: 8 + i copies the sign of byte i).
+__device__ __forceinline__ uint32_t pair_mask_bits(uint32_t bits, int c) {
+  const uint32_t s = bits << (c >> 1);
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(s), "r"((c & 1) ? 0xBBAAu : 0x9988u));
+  return r;
+}
+
+// Decision for key e (0..31) of a word made by keep_bits32.
+__device__ __forceinline__ bool keep_bit(uint32_t bits, int e) {
+  return (bits >> (8 * (e & 3) + 7 - (e >> 2))) & 1u;
 }
 
 // 16 x 16 byte transpose across the 16 lanes of a half-warp. Lane p holds row
@@ -92,11 +122,6 @@ __device__ __forceinline__ void transpose16_bytes(uint32_t (&w)[4], int lane) {
       w[a + 1] = __byte_perm(w[a + 1], r, put1);
     }
   }
-}
-
-// Four keep bytes (0xff / 0x00) -> four bits, byte b -> bit b.
-__device__ __forceinline__ uint32_t keep_nibble(uint32_t m) {
-  return ((m & 0x01010101u) * 0x01020408u) >> 24;
 }
 
 }  // namespace fa
