@@ -243,10 +243,14 @@ bool encode_f32_rows(CUtensorMap* map, const void* base, int BH, int rows, int d
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                                  static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d) * 4};
-  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(kBlock), 1};
+  // d = 64: 128 rows x 32 columns (128-byte rows, 128-byte swizzle); d = 128:
+  // 32 rows x 16 columns (64-byte rows, 64-byte swizzle), one warp's box.
+  const bool narrow = d == 128;
+  const cuuint32_t box[3] = {narrow ? 16u : 32u, narrow ? 32u : static_cast<cuuint32_t>(kBlock), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -22,9 +22,9 @@
 //                       dV_j += P^T dO_i
 //                       dS^T = P^T * (dP^T - D_i), bf16 -> shared memory
 //                       dK_j += dS^T Q_i
-//                       dQ_i  = dS K_j      TMEM -> shared memory (fp32) -> one
-//                              TMA bulk reduce-add per 32-column chunk into the
-//                              fp32 workspace accumulator
+//                       dQ_i += scale dS K_j  TMEM -> shared memory (fp32) -> TMA
+//                              bulk reduce-adds into the fp32 workspace
+//                              accumulator
 //                     Warps 0-7 compute P and dS (warps w and w+4 share the
 //                     key rows of TMEM lane quarter w % 4 and split the 128
 //                     query columns), warp 8 issues TMA, warp 9 issues
@@ -56,16 +56,20 @@ struct BwdLayout {
   static constexpr int kKVS = (D == 64) ? 2 : 1;     // K/V stages (next item's K/V prefetched)
   static constexpr int kQS = 2;                      // Q (+ LSE2 / D) stages
   static constexpr int kDS = (D == 64) ? 2 : 1;      // dO stages
-  static constexpr int kDQChunks = (D == 64) ? 2 : 1;  // 128 x 32 fp32 chunks staged at once
+  static constexpr int kDQChunks = 2;  // d = 64: 128 x 32 fp32 chunks staged at once
+  // d = 128: per drain warp a ring of kDQRing boxes of 32 rows x 16 fp32 columns
+  static constexpr int kDQRing = 3, kDQBox = 32 * 64;
+  static constexpr int kDQBytes = (D == 64) ? kDQChunks * kChunk : 4 * kDQRing * kDQBox;
   static constexpr int kKV = 0;                      // stage s: K at kKV + 2 s kTile, then V
   static constexpr int kQ = kKV + 2 * kKVS * kTile;
   static constexpr int kDO = kQ + kQS * kTile;
   static constexpr int kStat = kDO + kDS * kTile;    // per Q stage: lse2[128], delta[128]
   static constexpr int kDSb = kStat + kQS * 1024;    // dS^T, bf16, 2 chunks
-  static constexpr int kDQ = kDSb + 2 * kChunk;      // dQ staging (fp32, 128-byte swizzle)
-  static constexpr int kBar = kDQ + kDQChunks * kChunk;
+  static constexpr int kDQ = kDSb + 2 * kChunk;      // dQ staging (fp32, swizzled)
+  static constexpr int kBar = kDQ + kDQBytes;
   static constexpr int kEnd = kBar + 512 + 14 * 128;  // barriers etc.; tile lists of the 14 warps
   static constexpr int kSmem = kEnd + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
   // TMEM columns
   static constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256, kTDK = 256 + D;
   static constexpr uint32_t kTDQ = (D == 64) ? 384 : 128;  // d=128: dQ reuses the dP^T columns
@@ -583,7 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint8_t* stage = smem + L::kDQ;
     const uint32_t st_base = smem_u32(stage);
-    const bool issuer = (quarter == 0 && lane == 0);
+    // d = 128: every drain warp issues its own reduce-adds from its own ring
+    uint8_t* ring = stage + quarter * (L::kDQRing * L::kDQBox);
+    const uint32_t ring_base = smem_u32(ring);
+    const bool issuer = lane == 0 && (D == 128 || quarter == 0);
     constexpr int kRounds = (D / 32) / L::kDQChunks;
     int gq = 0, t = 0;
     bool ok = true;
@@ -627,6 +634,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_dqfree);
+        if constexpr (D == 128) {
+          // Each warp reduces its own 32 rows, in boxes of 16 columns staged
+          // through a ring of kDQRing buffers of its own: a box is written
+          // while the reduce-adds of the previous ones still read theirs, and
+          // no barrier across warps is needed. Rows are 64 bytes with the
+          // 64-byte swizzle (16-byte chunk u of row r at u ^ ((r >> 1) & 3)),
+          // so each 8-lane phase of a 16-byte store covers all 32 banks.
+          const uint32_t sw = (lane >> 1) & 3;
+#pragma unroll
+          for (int b = 0; b < D / 16; ++b) {
+            // Slots 0,1,2,0,1,2,0,1 in every tile. Before box b the reduce-add
+            // that last read its slot is done: box b-3 of this tile (two
+            // later groups may still read), or box 6 / 7 of the previous
+            // tile for boxes 0 / 1 (one later group may), or box 5 of the
+            // previous tile for box 2 (four later groups may).
+            const int slot = b % L::kDQRing;
+            if (lane == 0) {
+              if (b < 2)
+                bulk_wait_read<1>();
+              else
+                bulk_wait_read<2>();
+            }
+            __syncwarp();
+            const uint32_t* src = &v[b >> 1][(b & 1) * 16];
+            const uint32_t dst = ring_base + slot * L::kDQBox + lane * 64;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              st_shared_v4(dst + ((u ^ sw) << 4), __float_as_uint(__uint_as_float(src[4 * u]) * scale),
+                           __float_as_uint(__uint_as_float(src[4 * u + 1]) * scale),
+                           __float_as_uint(__uint_as_float(src[4 * u + 2]) * scale),
+                           __float_as_uint(__uint_as_float(src[4 * u + 3]) * scale));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_3d(&tm_dqacc, ring + slot * L::kDQBox, b * 16, i * kBlock + quarter * 32, x.bh);
+              bulk_commit();
+            }
+          }
+          continue;
+        }
 #pragma unroll
         for (int round = 0; round < kRounds; ++round) {
 #pragma unroll

@@ -93,6 +93,7 @@ struct FwdLayout {
   // list per warp (at most 12 warps)
   static constexpr int kEnd = kBar + 512 + 12 * 128;
   static constexpr int kSmem = kEnd + 1024;  // slack for 1024-byte alignment
+  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
   static constexpr uint32_t kTO = 256;       // O_A; O_B at kTO + D
   // P_t (bf16 pairs, 64 columns): its own columns, or over the first 64 of S_t
   static constexpr uint32_t kTP = kSepP ? 256 + 2 * D : 0;

@@ -182,7 +182,8 @@ struct FwdLaunch {
 struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // as above (4-D, the call's strides)
   CUtensorMap tm_dk, tm_dv;             // the outputs, same form (stores of whole tiles)
-  CUtensorMap tm_dqacc;  // fp32 [B*H, Npad, d] accumulator, box 32 x 128 x 1, 128B swizzle
+  CUtensorMap tm_dqacc;  // fp32 [B*H, Npad, d] accumulator; box 32 x 128 x 1, 128B swizzle
+                         // (d = 64) or 16 x 32 x 1, 64B swizzle (d = 128)
   const void* o;
   const void* dout;
   const float* lse;
