@@ -9,7 +9,7 @@
 //   D = rowsum(dO * O) (= rowsum(P * dP)),   dS = P * (dP - D),
 //   dQ = scale * dS K,   dK = scale * dS^T Q.
 //
-// 1. bwd_pre_kernel   D = rowsum(dO * O), LSE * log2(e), zero the fp32 dQ
+// 1. bwd_pre_kernel   D = rowsum(dO * O), -LSE * log2(e), zero the fp32 dQ
 //                     accumulator (bandwidth-bound, 16-byte accesses).
 // 2. bwd_main_kernel  persistent, one CTA per SM; a work item is one 128-key
 //                     tile j of one (batch, head). K_j and V_j stay in shared
@@ -139,10 +139,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (part == 0) {
         delta[row] = valid ? acc : 0.f;
-        float l2 = INFINITY;  // padding rows and rows that saw no key get P = 0
+        float l2 = -INFINITY;  // padding rows and rows that saw no key get P = 0
         if (valid) {
           const float v = lse[static_cast<size_t>(bh) * N + n];
-          if (v != -INFINITY) l2 = v * kLog2e;
+          if (v != -INFINITY) l2 = -(v * kLog2e);
         }
         lse2[row] = l2;
       }
@@ -862,13 +862,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // unpacks it, which halves the registers a compute thread holds.
         const bool diag = CAUSAL && i == x.j;
         uint32_t pk[32];
+        const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(st_lse + c);
-          float p0 = ex2(fmaf(__uint_as_float(rr[c >> 5][(c + 0) & 31]), scale_log2, -l4.x));
-          float p1 = ex2(fmaf(__uint_as_float(rr[c >> 5][(c + 1) & 31]), scale_log2, -l4.y));
-          float p2 = ex2(fmaf(__uint_as_float(rr[c >> 5][(c + 2) & 31]), scale_log2, -l4.z));
-          float p3 = ex2(fmaf(__uint_as_float(rr[c >> 5][(c + 3) & 31]), scale_log2, -l4.w));
+          const float4 l4 = *reinterpret_cast<const float4*>(st_lse + c);  // -LSE2
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[c >> 5][(c + 0) & 31]),
+                                   __uint_as_float(rr[c >> 5][(c + 1) & 31])),
+                           sc2, f2_pack(l4.x, l4.y)),
+                    x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rr[c >> 5][(c + 2) & 31]),
+                                   __uint_as_float(rr[c >> 5][(c + 3) & 31])),
+                           sc2, f2_pack(l4.z, l4.w)),
+                    x2, x3);
+          float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
           if (diag) {  // query i*128+qc0+c < key j*128+kr
             if (qc0 + c + 0 < kr) p0 = 0.f;
             if (qc0 + c + 1 < kr) p1 = 0.f;
@@ -916,13 +923,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
           float gv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
+          for (int e = 0; e < 8; e += 2) {  // pairs of columns (f32x2)
             const uint32_t w = pk[(q0 + e) >> 1];
-            const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
-            float dpe = __uint_as_float(rr[(q0 + e) >> 5][(q0 + e) & 31]);
-            if constexpr (DROP)
-              dpe = keep_bit(kb[(q0 + e) >> 5], (q0 + e) & 31) ? dpe * dp.rescale : 0.f;
-            gv[e] = pe * (dpe - dd[e]);
+            float dpe[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              dpe[h] = __uint_as_float(rr[(q0 + e + h) >> 5][(q0 + e + h) & 31]);
+              if constexpr (DROP)
+                dpe[h] = keep_bit(kb[(q0 + e + h) >> 5], (q0 + e + h) & 31) ? dpe[h] * dp.rescale : 0.f;
+            }
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
+                             f2_sub(f2_pack(dpe[0], dpe[1]), f2_pack(dd[e], dd[e + 1]))),
+                      gv[e], gv[e + 1]);
           }
           const uint32_t addr = ds_base + kr * 128 + (((u ^ (kr & 7))) << 4);
           st_shared_v4(addr, pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),

@@ -807,22 +807,39 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         // formed -- in its own columns, or over the first 64 columns of S_t,
         // whose fp32 values are already in registers -- so that few packed
         // words are live at once.
+        // At d = 128 the scale, shift and row sum work on pairs of columns
+        // (f32x2: half the instructions; the d = 64 variants measured slower
+        // with it, their register allocation being tighter).
+        const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_use, -m_use);
+        uint64_t ps2[2] = {0ull, 0ull};  // (+0, +0)
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 16) {
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const float p0 = ex2(fmaf(sv[2 * (c0 + c)], scale_log2, -m_use));
-            const float p1 = ex2(fmaf(sv[2 * (c0 + c) + 1], scale_log2, -m_use));
-            pk[c] = pack_bf16(p0, p1);
-            ps[c & 3] += p0 + p1;
+            if constexpr (D == 128) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(sv[2 * (c0 + c)], sv[2 * (c0 + c) + 1]), sc2, nm2), x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              pk[c] = pack_bf16(p0, p1);
+              ps2[c & 1] = f2_add(ps2[c & 1], f2_pack(p0, p1));
+            } else {
+              const float p0 = ex2(fmaf(sv[2 * (c0 + c)], scale_log2, -m_use));
+              const float p1 = ex2(fmaf(sv[2 * (c0 + c) + 1], scale_log2, -m_use));
+              pk[c] = pack_bf16(p0, p1);
+              ps[c & 3] += p0 + p1;
+            }
           }
           if constexpr (DROP) {  // keys j*128 + 2*c0 + [0, 32)
 #pragma unroll
             for (int c = 0; c < 16; ++c) pk[c] &= pair_mask_bits(kb[c0 >> 4], c);
           }
           tmem_st16(lane_base + p_col + c0, pk);
+        }
+        if constexpr (D == 128) {
+          f2_unpack(ps2[0], ps[0], ps[1]);
+          f2_unpack(ps2[1], ps[2], ps[3]);
         }
         const float tsum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         if (n >= 1 && __any_sync(0xffffffffu, grow)) {

@@ -196,7 +196,7 @@ struct BwdLaunch {
   float scale;
   const int32_t* kv_len;
   float* dq_acc;   // workspace: fp32 [B*H, Npad, d]
-  float* lse2;     // workspace: fp32 [B*H, Npad]  (LSE * log2 e; +inf on padding rows)
+  float* lse2;     // workspace: fp32 [B*H, Npad]  (-LSE * log2 e; -inf on padding rows)
   float* delta;    // workspace: fp32 [B*H, Npad]  (rowsum(dO * O); 0 on padding rows)
   const uint8_t* block_mask;  // device [nt][nt] (block-sparse backward) or nullptr
   void* split_ws;             // split area of the workspace (BwdSplitWorkspace), or nullptr
