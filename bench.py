@@ -59,10 +59,12 @@ def peaks():
 # digits of the SHA-256 of the kernel's source followed by the shared device
 # headers when it was captured; see profiles/).
 NCU_TRAFFIC = {
-    ("bwd_main", "gpt2_small"): (80_736_000, "fa_bwd_kernel.cuh", "b716048b0143a1e6"),
-    ("fwd", "gpt2_small"): (37_846_784, "fa_fwd_kernel.cuh", "e9c7433b2be3abe9"),
+    ("bwd_main", "long_n16384_noncausal"): (626_178_688, "fa_bwd_kernel.cuh", "5e184fc5969f424b"),
+    ("fwd", "long_n16384_noncausal"): (244_107_904, "fa_fwd_kernel.cuh", "66bea984c28cff10"),
+    ("bwd_main", "gpt2_small"): (79_388_544, "fa_bwd_kernel.cuh", "5e184fc5969f424b"),
+    ("fwd", "gpt2_small"): (37_817_344, "fa_fwd_kernel.cuh", "66bea984c28cff10"),
 }
-_SHARED_HEADERS = ("fa_ptx.cuh", "fa_philox.cuh", "fa_internal.h")
+_SHARED_HEADERS = ("fa_ptx.cuh", "fa_philox.cuh", "fa_internal.h", "fa_sched.cuh")
 
 
 def source_digest(src: str):
