@@ -875,15 +875,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    __uint_as_float(rr[c >> 5][(c + 3) & 31])),
                            sc2, f2_pack(l4.z, l4.w)),
                     x2, x3);
-          float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          if (diag) {  // query i*128+qc0+c < key j*128+kr
-            if (qc0 + c + 0 < kr) p0 = 0.f;
-            if (qc0 + c + 1 < kr) p1 = 0.f;
-            if (qc0 + c + 2 < kr) p2 = 0.f;
-            if (qc0 + c + 3 < kr) p3 = 0.f;
-          }
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
           pk[c / 2] = key_live ? pack_bf16(p0, p1) : 0u;
           pk[c / 2 + 1] = key_live ? pack_bf16(p2, p3) : 0u;
+        }
+        if (diag) {
+          // Causal diagonal tile: P = 0 where query i*128 + qc0 + c < key
+          // j*128 + kr. Applied to the packed pairs (column c in the low half
+          // of pk[c / 2] for even c) after the loop, which keeps the masking
+          // out of the loop's registers.
+          const int lim = kr - qc0;  // columns c < lim are masked
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            uint32_t m = 0xffffffffu;
+            if (c < lim) m &= 0xffff0000u;
+            if (c + 1 < lim) m &= 0x0000ffffu;
+            pk[c / 2] &= m;
+          }
         }
         // P^T over the first 32 of this warpgroup's 64 S^T columns (already read)
         if constexpr (DROP) {
