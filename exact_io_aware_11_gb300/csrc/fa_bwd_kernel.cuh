@@ -612,16 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      int w0 = (x.ts.begin & ~127) - 128, cnt = 0, idx = 0;  // window walk (block mask only)
+      // block mask: the kept Q tiles one after the other (inext: the next one)
+      int inext = MODE == kModeSparse ? next_kept(x.ts.mask, x.ts.stride, x.ts.begin, x.ts.end) : 0;
       for (int it = 0; it < x.n_iter; ++it, ++gq) {
         int i = x.ts.begin + it;
         if constexpr (MODE == kModeSparse) {
-          while (idx >= cnt) {
-            w0 += 128;
-            cnt = list_window(x.ts, w0, list);
-            idx = 0;
-          }
-          i = w0 + list[idx++];
+          i = inext;
+          inext = next_kept(x.ts.mask, x.ts.stride, i + 1, x.ts.end);
         }
         if (!mbar_wait_warp(bar_dqfull, gq & 1, wd)) { ok = false; break; }
         tc_fence_after();
@@ -805,16 +802,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (un.k < 0) break;
       const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
       const bool key_live = x.j * kBlock + kr < x.kv_bound;
-      int w0 = (x.ts.begin & ~127) - 128, cnt = 0, idx = 0;  // window walk (block mask only)
+      // block mask: the kept Q tiles one after the other (inext: the next one)
+      int inext = MODE == kModeSparse ? next_kept(x.ts.mask, x.ts.stride, x.ts.begin, x.ts.end) : 0;
       for (int it = 0; it < x.n_iter; ++it, ++gq) {
         int i = x.ts.begin + it;  // the Q tile (causal diagonal, dropout draws)
         if constexpr (MODE == kModeSparse) {
-          while (idx >= cnt) {
-            w0 += 128;
-            cnt = list_window(x.ts, w0, list);
-            idx = 0;
-          }
-          i = w0 + list[idx++];
+          i = inext;
+          inext = next_kept(x.ts.mask, x.ts.stride, i + 1, x.ts.end);
         }
         const int s = gq % QS;
         const float* st_lse = reinterpret_cast<const float*>(smem + L::kStat + s * 1024) + qc0;

@@ -872,13 +872,13 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
         return true;
       };
       if constexpr (MODE == kModeSparse) {
-        // Window by window (128 tiles): the mask row's kept tiles are listed
-        // in the warp's shared-memory list first.
-        for (int w0 = jbeg & ~127; ok && w0 < jend; w0 += 128) {
-          const int cnt =
-              list_window(TileSet{jbeg, jend, g.block_mask + static_cast<size_t>(qt) * g.nqt, 1}, w0, list);
-          for (int idx = 0; ok && idx < cnt; ++idx) ok = tile(w0 + list[idx]);
-          __syncwarp();  // the list may be rewritten for the next window
+        // The mask row's kept tiles one after the other; only the current
+        // tile and the next one stay live across the tile computation.
+        const uint8_t* mrow = g.block_mask + static_cast<size_t>(qt) * g.nqt;
+        for (int j = next_kept(mrow, 1, jbeg, jend); ok && j < jend;) {
+          const int jn = next_kept(mrow, 1, j + 1, jend);
+          ok = tile(j);
+          j = jn;
         }
       } else {
         for (int j = jbeg; ok && j < jend; ++j) ok = tile(j);

@@ -180,6 +180,22 @@ static __device__ __noinline__ int list_window(TileSet ts, int w0, uint8_t* list
   return base;
 }
 
+// The first tile >= j of [j, end) that the mask keeps (mask[c * stride] !=
+// 0; stride 1 walks a mask row, the number of tiles a column), or `end`:
+// 32 mask bytes per step, one per lane, and a ballot. Warp-collective. Out
+// of line for the same reason as list_window: its caller keeps only j and
+// the result live across the tile computation.
+static __device__ __noinline__ int next_kept(const uint8_t* __restrict__ mask, int stride, int j, int end) {
+  const int lane = threadIdx.x & 31;
+  for (int b = j; b < end; b += 32) {
+    const int c = b + lane;
+    const bool keep = c < end && __ldg(mask + static_cast<size_t>(c) * stride) != 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (bal != 0u) return b + __ffs(static_cast<int>(bal)) - 1;
+  }
+  return end;
+}
+
 // As list_window, for the union of two tile sets (the two Q tiles of a
 // forward item share their K/V loads).
 static __device__ __noinline__ int list_window2(TileSet a, TileSet b, int w0, uint8_t* list) {
