@@ -113,3 +113,28 @@ def test_sparse_bwd_full_size_workload(fa):
                           heads=heads)
     for b, h in heads:
         check_grads([f64(t)[b, h] for t in grads], [r[b, h] for r in ref], f"blocksparse bwd {(b, h)}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_sparse_kept_tiles_far_apart(fa, d):
+    """Every mask row and column keeps two blocks 33 tiles apart (the walks over
+    a mask scan 32 tiles per step): forward over all rows, backward of one head."""
+    N = 128 * 40
+    w = W.Workload("generic", 1, 2, N, d, causal=False, backward=True)
+    x = W.make_inputs(w, 41 + d)
+    nb = N // 128
+    mask = np.zeros((nb, nb), dtype=np.uint8)
+    for r in range(nb):
+        mask[r, r] = 1
+        mask[r, (r + 33) % nb] = 1
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    m = torch.from_numpy(mask).cuda()
+    o, lse = fa.blocksparse_forward(q, k, v, m, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, block_mask=mask)
+    check_fwd(o, lse, o_ref, l_ref, f"sparse far apart d={d}")
+    grads = _sparse_bwd(fa, x, mask, w.scale)
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, block_mask=mask,
+                          heads=[(0, 1)])
+    check_grads([f64(t)[0, 1] for t in grads], [r[0, 1] for r in ref], f"sparse far apart bwd d={d}")
