@@ -195,10 +195,10 @@ size_t span_bytes(int B, int H, int N, int d, const Strides& s, size_t elem) {
 // A bf16 [B, H, N, d] tensor with strides `st` as a tensor map: 3-D (d, N,
 // B*H) when st.merged, else 4-D with dimension 0 = d and dimensions 1..3 the
 // row, head and batch axes in the order st gives; box = 64 columns (128 bytes)
-// x 128 rows (x 1 x 1), 128-byte swizzle, zero fill outside the tensor
+// x box_rows rows (x 1 x 1), 128-byte swizzle, zero fill outside the tensor
 // (ragged N).
 bool encode_rows(CUtensorMap* map, const void* base, int B, int H, int N, int d,
-                 const Strides& st) {
+                 const Strides& st, int box_rows = kBlock) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   if (st.merged) {  // 3-D (d, N, B*H)
@@ -206,7 +206,7 @@ bool encode_rows(CUtensorMap* map, const void* base, int B, int H, int N, int d,
                                  static_cast<cuuint64_t>(B) * static_cast<cuuint64_t>(H)};
     const cuuint64_t strides3[2] = {static_cast<cuuint64_t>(st.n_map) * 2,
                                     static_cast<cuuint64_t>(st.bh) * 2};
-    const cuuint32_t box3[3] = {64, static_cast<cuuint32_t>(kBlock), 1};
+    const cuuint32_t box3[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr3[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims3, strides3,
               box3, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -226,7 +226,7 @@ bool encode_rows(CUtensorMap* map, const void* base, int B, int H, int N, int d,
   for (int a = 0; a < 3; ++a) {
     dims[1 + pos[a]] = static_cast<cuuint64_t>(ext[a]);
     strides[pos[a]] = static_cast<cuuint64_t>(ext[a] > 1 ? sv[a] : top) * 2;
-    box[1 + pos[a]] = a == 0 ? static_cast<cuuint32_t>(kBlock) : 1u;
+    box[1 + pos[a]] = a == 0 ? static_cast<cuuint32_t>(box_rows) : 1u;
   }
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
@@ -323,7 +323,7 @@ int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse,
   FwdLaunch a;
   std::memset(&a, 0, sizeof(a));
   if (!encode_rows(&a.tm_q, q, B, H, N, d, lay) || !encode_rows(&a.tm_k, k, B, H, N, d, lay) ||
-      !encode_rows(&a.tm_v, v, B, H, N, d, lay))
+      !encode_rows(&a.tm_v, v, B, H, N, d, lay) || !encode_rows(&a.tm_o, o, B, H, N, d, lay, 32))
     return FA_ERR_CUDA;
   a.st = lay;
   a.o = o;

@@ -92,7 +92,13 @@ struct FwdLayout {
   // barriers, TMEM address, abort flag, tail range; then one 128-byte tile
   // list per warp (at most 12 warps)
   static constexpr int kEnd = kBar + 512 + 12 * 128;
-  static constexpr int kSmem = kEnd + 1024;  // slack for 1024-byte alignment
+  // d = 64 (dense): per softmax warp a 32-row x 64-column bf16 box of O
+  // (128-byte swizzle) for the epilogue's TMA store. The head-paired
+  // block-sparse variant keeps row stores (measured slightly faster there).
+  static constexpr bool kOStore = (D == 64 && !kHP);
+  static constexpr int kOst = kEnd, kOBox = 32 * 128;
+  static constexpr int kOBytes = kOStore ? 8 * kOBox : 0;
+  static constexpr int kSmem = kOst + kOBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
   static constexpr uint32_t kTO = 256;       // O_A; O_B at kTO + D
   // P_t (bf16 pairs, 64 columns): its own columns, or over the first 64 of S_t
@@ -185,7 +191,8 @@ __device__ __forceinline__ int next_pair_tile(TileWalk<>& wa, TileWalk<>& wb, in
 template <int D, bool CAUSAL, bool DROP, int MODE>
 __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ out,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               __nv_bfloat16* __restrict__ out,
                float* __restrict__ lse_out, FwdGrid g, float scale_log2, DropoutParams dp,
                int* status, long long wait_limit) {
   // Block-sparse at d = 64: items pair one Q tile of two heads (same mask row),
@@ -926,6 +933,43 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       const bool live = have && l > 0.f;
       const float inv = live ? (DROP ? dp.rescale : 1.f) / l : 0.f;
       const bool row_ok = row < g.N;
+      if constexpr (L::kOStore) {
+        // The warp's 32 rows of O go to its shared-memory box (16-byte chunk
+        // u of row r at u ^ (r & 7)) and leave with one TMA store: whole
+        // 128-byte rows in full sectors, rows past N clipped.
+        uint8_t* obox = smem + L::kOst + (warp - kSoft0) * L::kOBox;
+        const uint32_t ob = smem_u32(obox) + lane * 128;
+        if (lane == 0) bulk_wait_read<0>();  // the previous item's store has read the box
+        __syncwarp();
+#pragma unroll
+        for (int c0 = 0; c0 < 2; ++c0) {
+          uint32_t o[32];
+          if (have) {
+            tmem_ld32(lane_base + o_col + c0 * 32, o);
+            tmem_wait_ld();
+            reg_fence(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            st_shared_v4(ob + (((c0 * 4 + v) ^ (lane & 7)) << 4),
+                         pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                         pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                         pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                         pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_rows(&tm_o, obox, 0, qt * kBlock + (warp & 3) * 32, bh, g.H, g.st);
+          bulk_commit();
+        }
+        if (row_ok)
+          lse_out[static_cast<size_t>(bh) * g.N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
+        continue;
+      }
       uint4* orow = reinterpret_cast<uint4*>(out + row_offset(g.st, g.H, bh, row));
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
@@ -952,6 +996,9 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       }
       if (row_ok)
         lse_out[static_cast<size_t>(bh) * g.N + row] = live ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+    if constexpr (L::kOStore) {  // the O stores have read their boxes and written O
+      if (lane == 0) bulk_wait0();
     }
   }
 
@@ -1036,7 +1083,7 @@ cudaError_t launch_fwd_kernel(const FwdLaunch& a, const FwdGrid& g, int grid, cu
   if (e != cudaSuccess) return e;
   const float scale_log2 = a.scale * 1.4426950408889634f;
   return launch_pdl(kern, dim3(grid), dim3(FwdWarps<D>::kThreads), L::kSmem, stream, a.tm_q, a.tm_k,
-                    a.tm_v, a.o, a.lse, g, scale_log2, a.drop, a.status, a.wait_limit);
+                    a.tm_v, a.tm_o, a.o, a.lse, g, scale_log2, a.drop, a.status, a.wait_limit);
 }
 
 // The split kernel over the tail on `grid` (= plan.tail_ctas) CTAs, then the

@@ -164,6 +164,7 @@ struct BwdGrid {
 
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v;  // 4-D maps (d, N, H, B) with the call's strides, box 64 x 128 x 1 x 1, 128B swizzle
+  CUtensorMap tm_o;              // O, the same layout, box 64 x 32 (one softmax warp's rows; d = 64 stores)
   void* split_ws;         // workspace for a split of the last wave, or nullptr
   size_t split_ws_bytes;
   void* o;
