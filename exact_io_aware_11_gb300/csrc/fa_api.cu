@@ -196,9 +196,11 @@ size_t span_bytes(int B, int H, int N, int d, const Strides& s, size_t elem) {
 // B*H) when st.merged, else 4-D with dimension 0 = d and dimensions 1..3 the
 // row, head and batch axes in the order st gives; box = 64 columns (128 bytes)
 // x box_rows rows (x 1 x 1), 128-byte swizzle, zero fill outside the tensor
-// (ragged N).
+// (ragged N); narrow = true: 32 columns (64 bytes) with the 64-byte swizzle.
 bool encode_rows(CUtensorMap* map, const void* base, int B, int H, int N, int d,
-                 const Strides& st, int box_rows = kBlock) {
+                 const Strides& st, int box_rows = kBlock, bool narrow = false) {
+  const cuuint32_t box_x = narrow ? 32u : 64u;
+  const CUtensorMapSwizzle swz = narrow ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   if (st.merged) {  // 3-D (d, N, B*H)
@@ -206,17 +208,17 @@ bool encode_rows(CUtensorMap* map, const void* base, int B, int H, int N, int d,
                                  static_cast<cuuint64_t>(B) * static_cast<cuuint64_t>(H)};
     const cuuint64_t strides3[2] = {static_cast<cuuint64_t>(st.n_map) * 2,
                                     static_cast<cuuint64_t>(st.bh) * 2};
-    const cuuint32_t box3[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+    const cuuint32_t box3[3] = {box_x, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr3[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims3, strides3,
-              box3, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              box3, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   }
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4];
   dims[0] = static_cast<cuuint64_t>(d);
-  box[0] = 64;
+  box[0] = box_x;
   const long long ext[3] = {N, H, B};
   const int pos[3] = {st.pn, st.ph, st.pb};
   const long long sv[3] = {st.n, st.h, st.b};
@@ -230,7 +232,7 @@ bool encode_rows(CUtensorMap* map, const void* base, int B, int H, int N, int d,
   }
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -415,8 +417,8 @@ int bwd_common(int stages, const BwdPtrs& p, int B, int H, int N, int d, int cau
                  !encode_rows(&a.tm_k, p.k, B, H, N, d, lay) ||
                  !encode_rows(&a.tm_v, p.v, B, H, N, d, lay) ||
                  !encode_rows(&a.tm_do, p.dout, B, H, N, d, lay) ||
-                 !encode_rows(&a.tm_dk, p.dk, B, H, N, d, lay) ||
-                 !encode_rows(&a.tm_dv, p.dv, B, H, N, d, lay) ||
+                 !encode_rows(&a.tm_dk, p.dk, B, H, N, d, lay, d == 128 ? 32 : kBlock, d == 128) ||
+                 !encode_rows(&a.tm_dv, p.dv, B, H, N, d, lay, d == 128 ? 32 : kBlock, d == 128) ||
                  !encode_f32_rows(&a.tm_dqacc, wsb + ws.dq_off, B * H, npad, d)))
     return FA_ERR_CUDA;
   a.st = lay;

@@ -740,20 +740,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         if constexpr (D == 128) {
-          // d = 128: straight from the registers to global memory, one row
-          // per thread. (The staged path below costs this variant more in
-          // the registers its dQ drain already keeps at the limit than the
-          // stores gain.)
-          if (key < N) {
-            uint4* dst = reinterpret_cast<uint4*>((which == 0 ? dv : dk) + out_off);
+          // d = 128: two boxes of 32 rows x 32 columns (bf16, 64-byte rows,
+          // 64-byte swizzle) per 64-column half, through the warp's dQ ring
+          // with the same slot order as the dQ boxes (8 boxes an item: the
+          // slots of the next tile's first boxes stay where its waits expect
+          // them), each written with one TMA store.
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const uint32_t* s = &a[u >> 2][(u & 3) * 8];
-              dst[h * 8 + u] = make_uint4(
-                  pack_bf16(__uint_as_float(s[0]) * mul, __uint_as_float(s[1]) * mul),
-                  pack_bf16(__uint_as_float(s[2]) * mul, __uint_as_float(s[3]) * mul),
-                  pack_bf16(__uint_as_float(s[4]) * mul, __uint_as_float(s[5]) * mul),
-                  pack_bf16(__uint_as_float(s[6]) * mul, __uint_as_float(s[7]) * mul));
+          for (int bb = 0; bb < 2; ++bb) {
+            const int e = oc * 2 + bb;  // 0..7
+            const int slot = e % L::kDQRing;
+            if (lane == 0) {
+              if (e < 2)
+                bulk_wait_read<1>();
+              else
+                bulk_wait_read<2>();
+            }
+            __syncwarp();
+            const uint32_t dst = ring_base + slot * L::kDQBox + lane * 64;
+            const uint32_t sw = (lane >> 1) & 3;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t* s = &a[bb][u * 8];
+              st_shared_v4(dst + ((u ^ sw) << 4),
+                           pack_bf16(__uint_as_float(s[0]) * mul, __uint_as_float(s[1]) * mul),
+                           pack_bf16(__uint_as_float(s[2]) * mul, __uint_as_float(s[3]) * mul),
+                           pack_bf16(__uint_as_float(s[4]) * mul, __uint_as_float(s[5]) * mul),
+                           pack_bf16(__uint_as_float(s[6]) * mul, __uint_as_float(s[7]) * mul));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_rows(which == 0 ? &tm_dv : &tm_dk, ring + slot * L::kDQBox, h * 64 + bb * 32,
+                             x.j * kBlock + quarter * 32, x.bh, grid.H, grid.st);
+              bulk_commit();
             }
           }
           continue;
