@@ -19,6 +19,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
+# The checked variant (-DFA_CHECKS=1: device-side checks of every TMA copy's
+# coordinates and addresses, reported as FA_ERR_DEVICE_CHECK) for tests.
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libfa_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -41,15 +45,15 @@ def _deps() -> list[str]:
             + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def _compile(src: str, extra: list[str]) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], build_dir: str = BUILD) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -57,27 +61,33 @@ def _compile(src: str, extra: list[str]) -> tuple[str, str]:
     return obj, r.stdout + r.stderr
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile every csrc/*.cu and link libfa.so. Returns the library path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    """Compile every csrc/*.cu and link libfa.so (libfa_checked.so with
+    checked=True). Returns the library path."""
+    lib_path = LIB_CHECKED if checked else LIB
+    build_dir = BUILD_CHECKED if checked else BUILD
+    if not force and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if checked:
+        extra.append("-DFA_CHECKS=1")
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
     if verbose_ptxas:
         for _, log in results:
             sys.stdout.write(log)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv,
+                checked="--checked" in sys.argv))

@@ -678,6 +678,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    case FA_ERR_DEVICE_CHECK: return "FA_ERR_DEVICE_CHECK";
     default: return "FA_UNKNOWN_STATUS";
   }
 }

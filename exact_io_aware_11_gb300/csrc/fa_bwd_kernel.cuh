@@ -82,6 +82,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
                                                   int y, int z) {
+  if (FA_CHECK_FAILS((x & 3) == 0 && x >= 0 && y >= 0 && z >= 0 && (smem_u32(src) & 127u) == 0)) return;
   asm volatile(
       "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
       " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
@@ -308,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  check_init(status);
   const int N = grid.N;
   const float scale_log2 = scale * kLog2e;
 

@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  check_init(status);
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {

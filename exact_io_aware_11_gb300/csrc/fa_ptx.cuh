@@ -190,8 +190,35 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 
 // 3-D tiled load (x = innermost, in elements) into shared memory; completion
 // is signalled on `bar` as transaction bytes.
+// Checked builds (compiled with -DFA_CHECKS=1; build(checked=True)): every
+// TMA copy first checks its coordinates and addresses -- the innermost
+// coordinate a multiple of 16 bytes, no negative coordinate for a store or a
+// reduction, shared-memory addresses 128-byte aligned, bulk copies of whole
+// 16-byte units. A failed check records FA_ERR_DEVICE_CHECK (5) in the status
+// word and skips the copy; the wait for a skipped load then gives up, bounded,
+// so the kernel returns instead of faulting. The kernels that issue TMA
+// copies hand the status word's address to check_init at their start.
+#ifndef FA_CHECKS
+#define FA_CHECKS 0
+#endif
+#if FA_CHECKS
+static __device__ int* g_check_status;  // one per translation unit
+static __device__ __forceinline__ void check_init(int* status) {
+  if (threadIdx.x == 0) g_check_status = status;  // before the kernel's first __syncthreads
+}
+static __device__ __noinline__ bool check_failed() {
+  if (g_check_status != nullptr) atomicCAS(g_check_status, 0, 5);
+  return true;
+}
+#define FA_CHECK_FAILS(cond) (!(cond) && check_failed())
+#else
+__device__ __forceinline__ void check_init(int*) {}
+#define FA_CHECK_FAILS(cond) false
+#endif
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y, int z) {
+  if (FA_CHECK_FAILS((x & 7) == 0 && (smem_u32(dst) & 127u) == 0 && (smem_u32(bar) & 7u) == 0)) return;
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
@@ -202,6 +229,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
 // 4-D tiled load (x = innermost, in elements) into shared memory.
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int x, int y, int z, int w) {
+  if (FA_CHECK_FAILS((x & 7) == 0 && (smem_u32(dst) & 127u) == 0 && (smem_u32(bar) & 7u) == 0)) return;
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
@@ -227,6 +255,7 @@ __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map,
 // and rows beyond the tensor's extent are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y,
                                              int z) {
+  if (FA_CHECK_FAILS((x & 7) == 0 && x >= 0 && y >= 0 && z >= 0 && (smem_u32(src) & 127u) == 0)) return;
   asm volatile(
       "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
@@ -235,6 +264,8 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 }
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int x, int y,
                                              int z, int w) {
+  if (FA_CHECK_FAILS((x & 7) == 0 && x >= 0 && y >= 0 && z >= 0 && w >= 0 && (smem_u32(src) & 127u) == 0))
+    return;
   asm volatile(
       "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
@@ -274,6 +305,9 @@ __device__ __forceinline__ void bulk_wait0() {
 // Untiled bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
+  if (FA_CHECK_FAILS((smem_u32(dst) & 15u) == 0 && (reinterpret_cast<uint64_t>(src) & 15u) == 0 &&
+                     (bytes & 15u) == 0 && (smem_u32(bar) & 7u) == 0))
+    return;
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
           "r"(smem_u32(dst)),

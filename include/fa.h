@@ -56,7 +56,8 @@ typedef enum {
   FA_ERR_INVALID_ARG = 1,
   FA_ERR_UNSUPPORTED = 2,
   FA_ERR_CUDA = 3,
-  FA_ERR_DEVICE_TIMEOUT = 4
+  FA_ERR_DEVICE_TIMEOUT = 4,
+  FA_ERR_DEVICE_CHECK = 5  /* checked builds only: a device-side bounds / alignment check failed */
 } fa_status;
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
@@ -308,7 +309,9 @@ int fa_attention_bwd(const void* q, const void* k, const void* v, const void* o,
                      size_t workspace_bytes, struct CUstream_st* stream);
 
 /* Device-side status of the current device: FA_OK, or FA_ERR_DEVICE_TIMEOUT
- * if a bounded wait inside a kernel gave up since the last call. Reading
+ * if a bounded wait inside a kernel gave up since the last call, or (in a
+ * library built with FA_CHECKS=1) FA_ERR_DEVICE_CHECK if a TMA copy failed
+ * its coordinate or alignment check and was skipped. Reading
  * clears it. Call only after synchronising the streams that ran the
  * kernels. Returns FA_ERR_CUDA if the status word cannot be read. */
 int fa_device_status(void);

@@ -51,7 +51,20 @@ def test_status_strings(L):
     import exact_io_aware_11_gb300 as fa
     assert fa.status_string(0) == "FA_OK"
     assert fa.status_string(4) == "FA_ERR_DEVICE_TIMEOUT"
+    assert fa.status_string(5) == "FA_ERR_DEVICE_CHECK"
     assert fa.status_string(99) == "FA_UNKNOWN_STATUS"
+
+
+def test_checked_build_exports_every_declared_symbol():
+    """The FA_CHECKS build (device-side checks of every TMA copy) compiles and
+    exports the same boundary; the GPU test runs it."""
+    from exact_io_aware_11_gb300 import build
+    path = build.build(checked=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\sT\s(fa_\w+)$", out, flags=re.M))
+    missing = [n for n in declared_symbols() if n not in exported]
+    assert not missing, missing
 
 
 def test_workspace_bytes_is_linear_in_n(L):
