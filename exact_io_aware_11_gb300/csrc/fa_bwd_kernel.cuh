@@ -67,7 +67,8 @@ struct BwdLayout {
   static constexpr int kDSb = kStat + kQS * 1024;    // dS^T, bf16, 2 chunks
   static constexpr int kDQ = kDSb + 2 * kChunk;      // dQ staging (fp32, swizzled)
   static constexpr int kBar = kDQ + kDQBytes;
-  static constexpr int kEnd = kBar + 512 + 14 * 128;  // barriers etc.; tile lists of the 14 warps
+  // barriers etc.; the producer's tile list; the cost-sorted group table
+  static constexpr int kEnd = kBar + 512 + 128 + 2 * kOrderMax;
   static constexpr int kSmem = kEnd + 1024;
   static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
   // TMEM columns
@@ -200,11 +201,18 @@ __host__ __device__ __forceinline__ int bwd_steps(const BwdGrid& g, int k) {
 
 // Unit u's item. With a block mask, counting the kept Q tiles is
 // warp-collective, so every lane of the calling warp must take part.
+// `order`: the cost-sorted group table (fa_sched.cuh) or null (index order).
 template <bool CAUSAL, int MODE>
-__device__ __forceinline__ BwdItem make_bwd_item(const BwdGrid& g, const Unit& u) {
+__device__ __forceinline__ BwdItem make_bwd_item(const BwdGrid& g, const Unit& u, const uint16_t* order) {
   constexpr bool SPARSE = MODE == kModeSparse;
   BwdItem x;
-  bwd_item_coords(g.nt, g.BH, CAUSAL, u.k, x.bh, x.j);
+  if (!SPARSE || order == nullptr) {
+    bwd_item_coords(g.nt, g.BH, CAUSAL, u.k, x.bh, x.j);
+  } else {  // groups: key tiles; members: (batch, head)
+    const int grp = u.k / g.BH;
+    x.j = order[grp];
+    x.bh = u.k - grp * g.BH;
+  }
   x.slot = u.slot;
   x.kv_bound = g.N;
   if (g.kv_len != nullptr) x.kv_bound = min(g.N, max(0, g.kv_len[x.bh / g.H]));
@@ -228,14 +236,14 @@ struct BwdCursor {
   int r = 0, it = 0, n = 0, t = 0, g = 0;
   bool valid = false;
   template <typename UnitFn>
-  __device__ void seek(const BwdGrid& G, UnitFn unit) {
+  __device__ void seek(const BwdGrid& G, UnitFn unit, const uint16_t* order) {
     for (;; ++r) {
       const Unit u = unit(r);
       if (u.k < 0) {
         valid = false;
         return;
       }
-      const int n_iter = make_bwd_item<CAUSAL, MODE>(G, u).n_iter;
+      const int n_iter = make_bwd_item<CAUSAL, MODE>(G, u, order).n_iter;
       if (n_iter > 0) {
         n = n_iter;
         it = 0;
@@ -245,14 +253,39 @@ struct BwdCursor {
     }
   }
   template <typename UnitFn>
-  __device__ void next(const BwdGrid& G, UnitFn unit) {
+  __device__ void next(const BwdGrid& G, UnitFn unit, const uint16_t* order) {
     ++g;
     if (++it < n) return;
     ++t;
     ++r;
-    seek(G, unit);
+    seek(G, unit, order);
   }
 };
+
+// The cost-sorted item order of a block-sparse backward pass (fa_sched.cuh),
+// built by the whole CTA before any TMA load: the groups are key tiles, each
+// costing the Q tiles that keep it. `scratch` (>= 6656 bytes) is a tile
+// buffer that no copy has written yet; every thread of the CTA takes part.
+// (Key padding alone is not sorted: it gained 1-2 % on a BERT-like pass.)
+template <bool CAUSAL>
+__device__ __forceinline__ void bwd_sort_items(int nt, const int32_t* kv_len, const uint8_t* mask,
+                                               uint8_t* scratch, uint64_t* bars) {
+  const int G = kv_len == nullptr ? nt : 0;
+  if (G == 0 || G > kOrderMax) return;  // uniform over the CTA
+  int* cost = reinterpret_cast<int*>(scratch);
+  int* hist = cost + kOrderMax;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) cost[i] = 0;
+  __syncthreads();
+  for_kept_blocks(mask, nt, [&](int i, int j) {
+    if (!CAUSAL || i >= j) atomicAdd(&cost[j], 1);
+  });
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0)
+    sort_groups(cost, G, min(kCostMax, nt), hist, reinterpret_cast<uint16_t*>(bars + 64) + 64);
+  fence_proxy_async_smem();  // the scratch tile is next written by TMA
+  if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(bars + kOrderFlagWord) = 1;
+  __syncthreads();
+}
 
 // ----------------------------------------------------------------- main kernel
 // Persistent: one CTA per SM walks its items; barrier phases run on across
@@ -301,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(bars + 24);
   uint64_t* bar_dpfree = bars + 25;   // dP^T read out of TMEM (d = 64)
   TailRange* tail_sh = reinterpret_cast<TailRange*>(bars + 26);  // this CTA's share of a split tail
-  uint8_t* walk_list = reinterpret_cast<uint8_t*>(bars + 64);     // [warp][128] Q tiles of a window (sparse)
+  uint8_t* walk_list = reinterpret_cast<uint8_t*>(bars + 64);     // [128] the producer's Q tiles of a window (sparse)
+  // then [kOrderMax] cost-sorted groups from walk_list + 128 (item_order)
   // d = 64: dQ has TMEM columns of its own, so dP^T of the next Q tile can be
   // issued as soon as the compute warps have read dP^T of this one, ahead of
   // this tile's dK and dQ MMAs in the in-order tensor pipe.
@@ -339,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_final, 1);
     mbar_init(bar_dpfree, 8);
     *abort_flag = 0;
+    *reinterpret_cast<int*>(bars + kOrderFlagWord) = 0;  // index order unless sorted below
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -359,6 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
   grid_dep_launch();
   const Watchdog wd{wait_limit, status, abort_flag};
+  // Cost-sorted item order with a block mask (bwd_sort_items).
+  constexpr bool kSort = MODE == kModeSparse;
+  if constexpr (kSort) bwd_sort_items<CAUSAL>(grid.nt, grid.kv_len, grid.mask, smem + L::kKV, bars);
   // The r-th unit of this CTA, or a unit with k < 0: the split kernel runs
   // the CTA's run of the tail; the others whole items [0, plan.whole) in a
   // snake over the item list.
@@ -378,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // [begin, end); with one, each 128-tile window's kept tiles are listed in
   // the warp's shared-memory list. Returns the tiles of window w0 and sets
   // `base` (tile = base + idx) or lists them (tile = w0 + list[idx]).
-  uint8_t* list = walk_list + 128 * warp;
+  uint8_t* list = walk_list;  // the producer's (the only warp that lists tiles)
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
@@ -434,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
+        const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un, kSort ? item_order(bars) : nullptr);
         if (x.n_iter == 0) continue;
         if (lane == 0) ok = load_kv(x);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -449,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
+        const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un, kSort ? item_order(bars) : nullptr);
         if (x.n_iter == 0) continue;
         ok = load_kv(x);
         for (int it = 0; ok && it < x.n_iter; ++it) ok = load_q(x, x.ts.begin + it);
@@ -515,11 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       Cur cur;
-      cur.seek(grid, unit);
+      cur.seek(grid, unit, kSort ? item_order(bars) : nullptr);
       bool ok = cur.valid && kv_ready(cur) && issue_s(cur) && issue_dp(cur);
       while (ok && cur.valid) {
         Cur nx = cur;
-        nx.next(grid, unit);
+        nx.next(grid, unit, kSort ? item_order(bars) : nullptr);
         const int gq = cur.g;
         const bool first = cur.it == 0, last = cur.it == cur.n - 1;
         const uint64_t q_mn = desc_adv(q_mn0, (gq % QS) * L::kTile);
@@ -599,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; ok; ++r) {
       const Unit un = unit(r);
       if (un.k < 0) break;
-      const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
+      const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un, kSort ? item_order(bars) : nullptr);
       const int key = x.j * kBlock + row;
       const long long out_off = row_offset(grid.st, grid.H, x.bh, key);
       if (x.n_iter == 0) {  // no valid key in this tile: zero gradients
@@ -821,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; ok; ++r) {
       const Unit un = unit(r);
       if (un.k < 0) break;
-      const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un);
+      const BwdItem x = make_bwd_item<CAUSAL, MODE>(grid, un, kSort ? item_order(bars) : nullptr);
       const bool key_live = x.j * kBlock + kr < x.kv_bound;
       // block mask: the kept Q tiles one after the other (inext: the next one)
       int inext = MODE == kModeSparse ? next_kept(x.ts.mask, x.ts.stride, x.ts.begin, x.ts.end) : 0;

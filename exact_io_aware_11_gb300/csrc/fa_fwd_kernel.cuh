@@ -89,14 +89,14 @@ struct FwdLayout {
   static constexpr int kK = kQ + 2 * kQS * kTile; // K of ring x, slot s: kK + (x kKS + s) kTile
   static constexpr int kV = kK + kRings * kKS * kTile;
   static constexpr int kBar = kV + kRings * kVS * kTile;
-  // barriers, TMEM address, abort flag, tail range; then one 128-byte tile
-  // list per warp (at most 12 warps)
-  static constexpr int kEnd = kBar + 512 + 12 * 128;
+  // barriers, TMEM address, abort flag, tail range; then the producer's
+  // 128-byte tile list and the cost-sorted group table
+  static constexpr int kEnd = kBar + 512 + 128 + 2 * kOrderMax;
   // d = 64 (dense): per softmax warp a 32-row x 64-column bf16 box of O
   // (128-byte swizzle) for the epilogue's TMA store. The head-paired
   // block-sparse variant keeps row stores (measured slightly faster there).
   static constexpr bool kOStore = (D == 64 && !kHP);
-  static constexpr int kOst = kEnd, kOBox = 32 * 128;
+  static constexpr int kOst = (kEnd + 1023) & ~1023, kOBox = 32 * 128;  // swizzle atoms: 1024-byte aligned
   static constexpr int kOBytes = kOStore ? 8 * kOBox : 0;
   static constexpr int kSmem = kOst + kOBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
@@ -137,14 +137,25 @@ __host__ __device__ __forceinline__ int fwd_steps(const FwdGrid& g, int k) {
   return fwd_item_steps(g.nqt, g.npairs, g.n_items / g.npairs, CAUSAL, k);
 }
 
+// `order`: the cost-sorted group table (fa_sched.cuh) or null (index order).
 template <bool CAUSAL, bool kHP = false>
-__device__ FwdItem make_item(const FwdGrid& g, const Unit& u) {
+__device__ FwdItem make_item(const FwdGrid& g, const Unit& u, const uint16_t* order) {
   FwdItem it;
   it.k = u.k;
   it.slot = u.slot;
   if constexpr (kHP) {
     // Q tile r of heads 2 hp and 2 hp + 1 of batch b: one mask row for both.
-    const int HP = (g.H + 1) / 2, bhp = u.k / g.nqt, r = u.k - bhp * g.nqt;
+    // Sorted: the groups are mask rows, their members (batch, head pair).
+    const int HP = (g.H + 1) / 2;
+    int bhp, r;
+    if (order != nullptr) {
+      const int inner = g.n_items / g.nqt, grp = u.k / inner;
+      r = order[grp];
+      bhp = u.k - grp * inner;
+    } else {
+      bhp = u.k / g.nqt;
+      r = u.k - bhp * g.nqt;
+    }
     const int b = bhp / HP, hp = bhp - b * HP;
     it.bh = b * g.H + 2 * hp;
     it.bhB = 2 * hp + 1 < g.H ? it.bh + 1 : -1;
@@ -152,7 +163,13 @@ __device__ FwdItem make_item(const FwdGrid& g, const Unit& u) {
     it.qtB = it.bhB >= 0 ? r : -1;
   } else {
     int p;
-    fwd_item_coords(g.npairs, g.n_items / g.npairs, CAUSAL, u.k, it.bh, p);
+    if (order == nullptr) {
+      fwd_item_coords(g.npairs, g.n_items / g.npairs, CAUSAL, u.k, it.bh, p);
+    } else {  // groups: pairs p; members: (batch, head)
+      const int BH = g.n_items / g.npairs, grp = u.k / BH;
+      p = order[grp];
+      it.bh = u.k - grp * BH;
+    }
     it.bhB = it.bh;
     it.qtA = 2 * p;
     it.qtB = 2 * p + 1 < g.nqt ? 2 * p + 1 : -1;
@@ -179,6 +196,35 @@ __device__ __forceinline__ int next_pair_tile(TileWalk<>& wa, TileWalk<>& wb, in
   hA = a == m;
   hB = b == m;
   return m;
+}
+
+// The cost-sorted item order of a block-sparse forward pass (fa_sched.cuh),
+// built by the whole CTA before any TMA load: the groups are mask rows (kHP:
+// d = 64, head-paired items) or pairs of rows, a group's cost the number of
+// (Q tile, K/V tile) products of one of its items. `scratch` (>= 6656 bytes)
+// is a tile buffer that no copy has written yet; every thread of the CTA
+// takes part. (Key padding alone is not sorted: those items differ little in
+// cost -- a BERT-like pass's items took 6.6-7.2 us whatever their length --
+// and the sort's start-up cost more than it evened out.)
+template <bool CAUSAL, bool kHP>
+__device__ __forceinline__ void fwd_sort_items(int nqt, int npairs, const int32_t* kv_len,
+                                               const uint8_t* block_mask, uint8_t* scratch,
+                                               uint64_t* bars) {
+  const int G = kv_len == nullptr ? (kHP ? nqt : npairs) : 0;
+  if (G == 0 || G > kOrderMax) return;  // uniform over the CTA
+  int* cost = reinterpret_cast<int*>(scratch);
+  int* hist = cost + kOrderMax;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) cost[i] = 0;
+  __syncthreads();
+  for_kept_blocks(block_mask, nqt, [&](int r, int c) {
+    if (!CAUSAL || c <= r) atomicAdd(&cost[kHP ? r : r >> 1], 1);
+  });
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0)
+    sort_groups(cost, G, min(kCostMax, 2 * nqt), hist, reinterpret_cast<uint16_t*>(bars + 64) + 64);
+  fence_proxy_async_smem();  // the scratch tile is next written by TMA
+  if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(bars + kOrderFlagWord) = 1;
+  __syncthreads();
 }
 
 // DROP: inverted dropout on P (fa_philox.cuh); the row sums and LSE use the
@@ -218,7 +264,8 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::oTmem);
   int* abort_flag = reinterpret_cast<int*>(bars + L::oAbort);
   TailRange* tail_sh = reinterpret_cast<TailRange*>(bars + L::oTail);  // this CTA's share of a split tail
-  uint8_t* walk_list = reinterpret_cast<uint8_t*>(bars + 64);     // [warp][128] kept tiles of a window (sparse)
+  uint8_t* walk_list = reinterpret_cast<uint8_t*>(bars + 64);     // [128] the producer's kept tiles of a window (sparse)
+  // then [kOrderMax] cost-sorted groups from walk_list + 128 (item_order)
   constexpr int kMmaB = FwdWarps<D>::kMmaB, kSoft0 = FwdWarps<D>::kSoft0;
   // arrivals that release a K or V ring slot: both issuers at d = 64 when the
   // slots share one ring, else the one issuer that uses it
@@ -250,6 +297,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     mbar_init(bar_final, 1);
     mbar_init(bar_final + 1, 1);
     *abort_flag = 0;
+    *reinterpret_cast<int*>(bars + kOrderFlagWord) = 0;  // index order unless sorted below
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -270,6 +318,9 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   grid_dep_wait();  // the previous kernel's outputs (Q, K, V, O, ...) are complete
   grid_dep_launch();
   const Watchdog wd{wait_limit, status, abort_flag};
+  // Cost-sorted item order with a block mask (fwd_sort_items).
+  constexpr bool kSort = MODE == kModeSparse;
+  if constexpr (kSort) fwd_sort_items<CAUSAL, kHP>(g.nqt, g.npairs, g.kv_len, g.block_mask, smem + L::kQ, bars);
   // The r-th unit of this CTA, or a unit with k < 0: the split kernel runs
   // the CTA's run of the tail; the others whole items [0, plan.whole) in a
   // snake over the item list.
@@ -285,7 +336,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       return u;
     }
   };
-  uint8_t* list = walk_list + 128 * warp;
+  uint8_t* list = walk_list;  // the producer's (the only warp that lists tiles)
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -347,7 +398,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un, kSort ? item_order(bars) : nullptr);
         TileWalk<> wa;
         wa.init(it.tsA);
         const int lastA = wa.last(), lastB = it.bhB >= 0 ? lastA : -1;
@@ -371,7 +422,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un, kSort ? item_order(bars) : nullptr);
         TileWalk<> wa, wb;
         wa.init(it.tsA);
         wb.init(it.tsB);
@@ -391,7 +442,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un, kSort ? item_order(bars) : nullptr);
         const int lastA = it.tsA.end > it.tsA.begin ? it.tsA.end - 1 : -1;
         const int lastB = it.tsB.end > it.tsB.begin ? it.tsB.end - 1 : -1;
         ok = load_q(it, lastA, lastB);
@@ -470,7 +521,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un0 = unit(r);
         if (un0.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un0);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un0, kSort ? item_order(bars) : nullptr);
         TileWalk<> wa, wb;  // block-mask walks (sparse)
         wa.init(it.tsA);
         wb.init(it.tsB);
@@ -606,7 +657,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un0 = unit(r);
         if (un0.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un0);
+        const FwdItem it = make_item<CAUSAL, kHP>(g, un0, kSort ? item_order(bars) : nullptr);
         TileWalk<> wa, wb;  // block-mask walks (sparse)
         wa.init(it.tsA);
         wb.init(it.tsB);
@@ -734,7 +785,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     for (int ri = 0; ok; ++ri) {
       const Unit un0 = unit(ri);
       if (un0.k < 0) break;
-      const FwdItem it = make_item<CAUSAL, kHP>(g, un0);
+      const FwdItem it = make_item<CAUSAL, kHP>(g, un0, kSort ? item_order(bars) : nullptr);
       const int qt = t ? it.qtB : it.qtA;
       if (qt < 0) continue;
       const int jbeg = t ? it.tsB.begin : it.tsA.begin, jend = t ? it.tsB.end : it.tsA.end;

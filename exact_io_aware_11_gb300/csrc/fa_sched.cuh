@@ -214,6 +214,100 @@ static __device__ __noinline__ int list_window2(TileSet a, TileSet b, int w0, ui
   return base;
 }
 
+// ------------------------------------------------------------------ cost-sorted item order
+// With a block mask the items of a pass differ in cost, and dealing them out
+// in index order can leave some SMs with far more tiles than others (3 to 12
+// kept tiles per mask row: up to a third more than the average). Such items
+// form groups of equal cost -- a mask row or pair of rows (forward), a key
+// tile (backward) -- and at its start every CTA sorts the groups by
+// decreasing cost, ties by increasing index, into a table in shared memory
+// (the same table in every CTA); item k is then member k % inner of group
+// order[k / inner], and the snake over the item list deals out the heaviest
+// items first.
+constexpr int kOrderMax = 640;  // groups a table holds; with more, index order
+constexpr int kCostMax = 1023;  // costs above this sort as equal
+// Both persistent kernels keep, in 64-bit words from their barrier area, a
+// flag at word 40 (non-zero: the table is in use) and the table itself from
+// byte 640 (after the producer's 128-byte tile list at word 64).
+constexpr int kOrderFlagWord = 40;
+
+// The CTA's group table, or null for index order. Read from shared memory at
+// every item, so that no role keeps it live across its tile loops.
+__device__ __forceinline__ const uint16_t* item_order(const uint64_t* bars) {
+  const int on = *reinterpret_cast<const volatile int*>(bars + kOrderFlagWord);
+  return on ? reinterpret_cast<const uint16_t*>(bars + 64) + 64 : nullptr;
+}
+
+// Warp-collective: order[0, G) = the groups 0 .. G-1 by decreasing cost[]
+// (ties by increasing index); costs above maxc (<= kCostMax) count as maxc.
+// `hist` is scratch of maxc + 1 ints. A counting sort: histogram of the
+// costs, the first slot of every cost by a scan from the top, then the
+// groups placed 32 at a time (lanes of equal cost ranked by __match_any_sync).
+static __device__ __noinline__ void sort_groups(const int* cost, int G, int maxc, int* hist,
+                                                uint16_t* order) {
+  const int lane = threadIdx.x & 31;
+  for (int v = lane; v <= maxc; v += 32) hist[v] = 0;
+  __syncwarp();
+  for (int i = lane; i < G; i += 32) atomicAdd(&hist[min(cost[i], maxc)], 1);
+  __syncwarp();
+  int run = 0;  // groups costing more than the current chunk's top
+  for (int top = maxc; top >= 0; top -= 32) {
+    const int v = top - lane;
+    const int h = v >= 0 ? hist[v] : 0;
+    int x = h;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    __syncwarp();
+    if (v >= 0) hist[v] = run + x - h;
+    run += __shfl_sync(0xffffffffu, x, 31);
+  }
+  __syncwarp();
+  for (int base = 0; base < G; base += 32) {
+    const int i = base + lane;
+    const bool act = i < G;
+    const int v = act ? min(cost[i], maxc) : -1 - lane;  // inactive lanes match nobody
+    const unsigned peers = __match_any_sync(0xffffffffu, v);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int s = act ? hist[v] : 0;
+    if (act) order[s + rank] = static_cast<uint16_t>(i);
+    __syncwarp();
+    if (act && rank == 0) hist[v] = s + __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Block-wide: kept(r, c) for every non-zero byte mask[r n + c] of an n x n
+// block mask (16-byte loads when the mask's address and n allow them).
+template <typename Fn>
+__device__ __forceinline__ void for_kept_blocks(const uint8_t* __restrict__ mask, int n, Fn kept) {
+  if ((reinterpret_cast<uintptr_t>(mask) & 15u) == 0 && (n & 15) == 0) {
+    const int per_row = n >> 4, total = n * per_row;
+    const uint4* m4 = reinterpret_cast<const uint4*>(mask);
+    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+      const uint4 w = __ldg(m4 + idx);
+      const int r = idx / per_row, c0 = (idx - r * per_row) * 16;
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        // top bit of each byte: the byte is non-zero
+        uint32_t nz = (((ws[q] & 0x7f7f7f7fu) + 0x7f7f7f7fu) | ws[q]) & 0x80808080u;
+        while (nz != 0u) {
+          const int b = (__ffs(static_cast<int>(nz)) - 1) >> 3;
+          kept(r, c0 + 4 * q + b);
+          nz &= nz - 1u;
+        }
+      }
+    }
+  } else {
+    const int total = n * n;
+    for (int idx = threadIdx.x; idx < total; idx += blockDim.x)
+      if (__ldg(mask + idx) != 0) kept(idx / n, idx % n);
+  }
+}
+
 // ------------------------------------------------------------------ item plan
 // Fewest tail steps a CTA is given: a part costs a partial-result write and
 // the merge a read of it, which a part of one or two steps would not repay.
