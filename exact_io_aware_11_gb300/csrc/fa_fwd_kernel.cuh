@@ -138,7 +138,11 @@ __host__ __device__ __forceinline__ int fwd_steps(const FwdGrid& g, int k) {
 }
 
 // `order`: the cost-sorted group table (fa_sched.cuh) or null (index order).
-template <bool CAUSAL, bool kHP = false>
+// kAlt (causal, whole items): Q tile 2p + 1 sees one K/V tile more than 2p,
+// so the slot that takes it alternates from one round of items to the next
+// ((k / gridDim.x) odd: A = 2p + 1, B = 2p) -- otherwise slot B would carry
+// one tile more per item and finish a CTA's items several tiles after A.
+template <bool CAUSAL, bool kHP = false, bool kAlt = false>
 __device__ FwdItem make_item(const FwdGrid& g, const Unit& u, const uint16_t* order) {
   FwdItem it;
   it.k = u.k;
@@ -173,6 +177,10 @@ __device__ FwdItem make_item(const FwdGrid& g, const Unit& u, const uint16_t* or
     it.bhB = it.bh;
     it.qtA = 2 * p;
     it.qtB = 2 * p + 1 < g.nqt ? 2 * p + 1 : -1;
+    if (kAlt && it.qtB >= 0 && ((u.k / static_cast<int>(gridDim.x)) & 1)) {
+      it.qtA = 2 * p + 1;
+      it.qtB = 2 * p;
+    }
   }
   it.kv_bound = g.N;
   if (g.kv_len != nullptr) it.kv_bound = min(g.N, max(0, g.kv_len[it.bh / g.H]));
@@ -320,6 +328,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
   const Watchdog wd{wait_limit, status, abort_flag};
   // Cost-sorted item order with a block mask (fwd_sort_items).
   constexpr bool kSort = MODE == kModeSparse;
+  constexpr bool kAltSlots = CAUSAL && MODE == kModePlain;  // see make_item
   if constexpr (kSort) fwd_sort_items<CAUSAL, kHP>(g.nqt, g.npairs, g.kv_len, g.block_mask, smem + L::kQ, bars);
   // The r-th unit of this CTA, or a unit with k < 0: the split kernel runs
   // the CTA's run of the tail; the others whole items [0, plan.whole) in a
@@ -398,7 +407,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un, kSort ? item_order(bars) : nullptr);
+        const FwdItem it = make_item<CAUSAL, kHP, kAltSlots>(g, un, kSort ? item_order(bars) : nullptr);
         TileWalk<> wa;
         wa.init(it.tsA);
         const int lastA = wa.last(), lastB = it.bhB >= 0 ? lastA : -1;
@@ -422,7 +431,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un, kSort ? item_order(bars) : nullptr);
+        const FwdItem it = make_item<CAUSAL, kHP, kAltSlots>(g, un, kSort ? item_order(bars) : nullptr);
         TileWalk<> wa, wb;
         wa.init(it.tsA);
         wb.init(it.tsB);
@@ -442,7 +451,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un = unit(r);
         if (un.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un, kSort ? item_order(bars) : nullptr);
+        const FwdItem it = make_item<CAUSAL, kHP, kAltSlots>(g, un, kSort ? item_order(bars) : nullptr);
         const int lastA = it.tsA.end > it.tsA.begin ? it.tsA.end - 1 : -1;
         const int lastB = it.tsB.end > it.tsB.begin ? it.tsB.end - 1 : -1;
         ok = load_q(it, lastA, lastB);
@@ -521,7 +530,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un0 = unit(r);
         if (un0.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un0, kSort ? item_order(bars) : nullptr);
+        const FwdItem it = make_item<CAUSAL, kHP, kAltSlots>(g, un0, kSort ? item_order(bars) : nullptr);
         TileWalk<> wa, wb;  // block-mask walks (sparse)
         wa.init(it.tsA);
         wb.init(it.tsB);
@@ -657,7 +666,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
       for (int r = 0; ok; ++r) {
         const Unit un0 = unit(r);
         if (un0.k < 0) break;
-        const FwdItem it = make_item<CAUSAL, kHP>(g, un0, kSort ? item_order(bars) : nullptr);
+        const FwdItem it = make_item<CAUSAL, kHP, kAltSlots>(g, un0, kSort ? item_order(bars) : nullptr);
         TileWalk<> wa, wb;  // block-mask walks (sparse)
         wa.init(it.tsA);
         wb.init(it.tsB);
@@ -785,7 +794,7 @@ __global__ void __launch_bounds__(FwdWarps<D>::kThreads, 1)
     for (int ri = 0; ok; ++ri) {
       const Unit un0 = unit(ri);
       if (un0.k < 0) break;
-      const FwdItem it = make_item<CAUSAL, kHP>(g, un0, kSort ? item_order(bars) : nullptr);
+      const FwdItem it = make_item<CAUSAL, kHP, kAltSlots>(g, un0, kSort ? item_order(bars) : nullptr);
       const int qt = t ? it.qtB : it.qtA;
       if (qt < 0) continue;
       const int jbeg = t ? it.tsB.begin : it.tsA.begin, jend = t ? it.tsB.end : it.tsA.end;
