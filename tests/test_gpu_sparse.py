@@ -138,3 +138,40 @@ def test_sparse_kept_tiles_far_apart(fa, d):
     ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, block_mask=mask,
                           heads=[(0, 1)])
     check_grads([f64(t)[0, 1] for t in grads], [r[0, 1] for r in ref], f"sparse far apart bwd d={d}")
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, False), (64, True)])
+def test_sparse_skewed_costs(fa, d, causal):
+    """Mask rows and columns that keep very different numbers of blocks (the
+    items are dealt out heaviest first, from a per-CTA sort of the mask's rows
+    or columns): a diagonal, two full rows and two full columns, a row and a
+    column that keep nothing; more items than one wave of CTAs."""
+    N = 128 * 40
+    nb = N // 128
+    w = W.Workload("generic", 2, 4, N, d, causal=causal, backward=True)
+    x = W.make_inputs(w, 51 + d + int(causal))
+    mask = np.zeros((nb, nb), dtype=np.uint8)
+    np.fill_diagonal(mask, 1)
+    mask[5, :] = 1
+    mask[30, :] = 1
+    mask[:, 7] = 1
+    mask[:, 33] = 1
+    mask[12, :] = 0
+    mask[:, 20] = 0
+    q, k, v, do = cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), cuda(x["dout"])
+    m = torch.from_numpy(mask).cuda()
+    o, lse = fa.attention_forward(q, k, v, causal=causal, scale=w.scale, block_mask=m)
+    g = fa.attention_backward(q, k, v, o, do, lse, causal=causal, scale=w.scale, block_mask=m)
+    torch.cuda.synchronize()
+    assert fa.device_status() == 0
+    blocks = [0, 5, 7, 12, 30, 39]
+    rows = np.concatenate([np.arange(b * 128, (b + 1) * 128) for b in blocks])
+    o_ref, l_ref = oracle.forward(x["q"], x["k"], x["v"], w.scale, causal=causal, block_mask=mask,
+                                  rows=rows)
+    check_fwd(f64(o)[:, :, rows], f64(lse)[:, :, rows], o_ref, l_ref, f"skewed d={d} causal={causal}")
+    assert np.all(f64(o)[:, :, 12 * 128:13 * 128] == 0)
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["dout"], w.scale, causal=causal, block_mask=mask,
+                          heads=[(1, 2)])
+    check_grads([f64(t)[1, 2] for t in g], [r[1, 2] for r in ref], f"skewed bwd d={d} causal={causal}")
+    dk, dv = f64(g[1]), f64(g[2])
+    assert np.all(dk[:, :, 20 * 128:21 * 128] == 0) and np.all(dv[:, :, 20 * 128:21 * 128] == 0)
