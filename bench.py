@@ -59,10 +59,10 @@ def peaks():
 # digits of the SHA-256 of the kernel's source followed by the shared device
 # headers when it was captured; see profiles/).
 NCU_TRAFFIC = {
-    ("bwd_main", "long_n16384_noncausal"): (633_911_168, "fa_bwd_kernel.cuh", "57262a340078561a"),
-    ("fwd", "long_n16384_noncausal"): (245_179_392, "fa_fwd_kernel.cuh", "437ba0659646433b"),
-    ("bwd_main", "gpt2_small"): (78_426_624, "fa_bwd_kernel.cuh", "57262a340078561a"),
-    ("fwd", "gpt2_small"): (37_825_536, "fa_fwd_kernel.cuh", "437ba0659646433b"),
+    ("bwd_main", "long_n16384_noncausal"): (633_911_168, "fa_bwd_kernel.cuh", "616966a460650ff0"),
+    ("fwd", "long_n16384_noncausal"): (245_179_392, "fa_fwd_kernel.cuh", "bf39e8e345d091cf"),
+    ("bwd_main", "gpt2_small"): (78_426_624, "fa_bwd_kernel.cuh", "616966a460650ff0"),
+    ("fwd", "gpt2_small"): (37_825_536, "fa_fwd_kernel.cuh", "bf39e8e345d091cf"),
 }
 _SHARED_HEADERS = ("fa_ptx.cuh", "fa_philox.cuh", "fa_internal.h", "fa_sched.cuh")
 
@@ -209,11 +209,20 @@ class Step:
         self.offset = 0  # dropout counter offset, advanced once per step
 
     def launches(self):
-        """Kernels of one step: the forward (+ its merge when split), then the
-        backward's preprocess, main (+ merge when split) and dQ conversion."""
-        n = 1 + int(self.fwd_split)
-        if self.w.backward:
-            n += 3 + int(self.bwd_split)
+        """Kernels of one step: the forward, then the backward's preprocess,
+        main and dQ conversion. A pass split over its last wave runs its whole
+        rounds on the plain kernel (when there is at least one), the tail on
+        the split kernel and the merge of the cut items (counted as present)."""
+        w = self.w
+        G = torch.cuda.get_device_properties(self.q.device).multi_processor_count
+        nt = (w.N + 127) // 128
+
+        def split_pass(n_items):
+            return (1 if n_items >= G else 0) + 2
+
+        n = split_pass(w.B * w.H * ((nt + 1) // 2)) if self.fwd_split else 1
+        if w.backward:
+            n += 2 + (split_pass(w.B * w.H * nt) if self.bwd_split else 1)
         return n
 
     def fwd(self, stream):
